@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle: checks against what the pages and mathematics fix.
+
+Nothing here compares the oracle with a retyped copy of itself: the pins are the
+worked example printed on "FlashAttention, explained", brute force with plain
+Python loops, library routines (scipy softmax / logsumexp), closed forms and
+invariants.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+
+from oracle import attention as orc
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [float(x) for x in rest]
+    return vals
+
+
+def _rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------- T1 ----
+def test_worked_example_matches_printed_values():
+    """'FlashAttention, explained', worked example: row [2,1,3,0] in blocks [2,1],[3,0]."""
+    g = _golden("worked_example.txt")
+    m, l, w, hist = orc.softmax_row_blocked(g["scores"], int(g["block"][0]))
+    assert m == g["m"][0]
+    assert abs(l - g["l"][0]) <= 5e-5
+    assert np.max(np.abs(w - np.array(g["weights"]))) <= 5e-5
+    # logsumexp consistent with the printed m and l (l printed to 4 decimals)
+    assert abs((m + math.log(l)) - (g["m"][0] + math.log(g["l"][0]))) <= 5e-5 / 1.5
+
+
+def test_worked_example_intermediate_state():
+    """After block [2,1] the page's running state is m = 2 with every term e^{s-2}."""
+    _, _, _, hist = orc.softmax_row_blocked([2, 1, 3, 0], 2)
+    m1, l1 = hist[0]
+    assert m1 == 2.0
+    assert l1 == pytest.approx(1.0 + math.exp(-1.0), abs=1e-15)
+    # second block: old sum corrected by the single factor e^{2-3}
+    m2, l2 = hist[1]
+    assert m2 == 3.0
+    assert l2 == pytest.approx(l1 * math.exp(2 - 3) + math.exp(0) + math.exp(-3), abs=1e-15)
+
+
+def test_planted_mistake_is_caught_by_worked_example():
+    """Dropping the rescale factor (a plausible bug) breaks the printed l."""
+    s = np.array([2.0, 1.0, 3.0, 0.0])
+    m, l = -np.inf, 0.0
+    for blk in (s[:2], s[2:]):
+        m_new = max(m, blk.max())
+        l = l + np.exp(blk - m_new).sum()      # missing l * e^{m - m'}
+        m = m_new
+    assert abs(l - 1.5530) > 5e-5
+
+
+# ---------------------------------------------------------------- brute force ----
+def _python_attention(q, k, v, scale, causal):
+    """Textbook attention with plain Python loops (tiny inputs only)."""
+    nq, nk, dv = len(q), len(k), len(v[0])
+    out, lses = [], []
+    for i in range(nq):
+        scores = []
+        for j in range(nk):
+            if causal and j > i + (nk - nq):
+                continue
+            scores.append((j, scale * sum(q[i][c] * k[j][c] for c in range(len(q[i])))))
+        mx = max(s for _, s in scores)
+        ws = [(j, math.exp(s - mx)) for j, s in scores]
+        tot = sum(w for _, w in ws)
+        out.append([sum(w * v[j][c] for j, w in ws) / tot for c in range(dv)])
+        lses.append(mx + math.log(tot))
+    return np.array(out), np.array(lses)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("nq,nk,d", [(1, 1, 3), (3, 5, 4), (5, 5, 2), (7, 4, 3)])
+def test_definition_vs_python_loops(causal, nq, nk, d):
+    if causal and nq > nk:
+        pytest.skip("bottom-right causal with Nq > Nk leaves rows fully masked")
+    rng = np.random.default_rng(nq * 100 + nk * 10 + d)
+    q, k, v = _rand(rng, nq, d), _rand(rng, nk, d), _rand(rng, nk, d + 1)
+    o, lse = orc.attention_definition(q, k, v, 0.7, causal)
+    o_ref, lse_ref = _python_attention(q.tolist(), k.tolist(), v.tolist(), 0.7, causal)
+    assert np.max(np.abs(o - o_ref)) <= 1e-13
+    assert np.max(np.abs(lse - lse_ref)) <= 1e-13
+
+
+# ---------------------------------------------------------------- T2 ----
+@pytest.mark.parametrize("n", [1, 2, 3, 4, 5, 7, 8, 13, 17, 31, 64])
+@pytest.mark.parametrize("causal", [False, True])
+def test_blocked_equals_definition_for_every_block_size(n, causal):
+    """'Tiles and an online softmax': the blocked result is the full softmax, any block size."""
+    rng = np.random.default_rng(n + (1000 if causal else 0))
+    d = 8
+    q, k, v = _rand(rng, n, d), _rand(rng, n, d), _rand(rng, n, d)
+    o_ref, lse_ref = orc.attention_definition(q, k, v, 0.5, causal)
+    for bs in range(1, n + 1):
+        for fn in (orc.attention_blocked, orc.attention_blocked_normalised):
+            o, lse = fn(q, k, v, 0.5, causal, bs)
+            assert np.max(np.abs(o - o_ref)) <= 1e-12, (fn.__name__, bs)
+            assert np.max(np.abs(lse - lse_ref)) <= 1e-12, (fn.__name__, bs)
+
+
+def test_blocked_row_equals_library_softmax():
+    rng = np.random.default_rng(7)
+    s = rng.standard_normal(37) * 4
+    for bs in (1, 2, 5, 37):
+        m, l, w, _ = orc.softmax_row_blocked(s, bs)
+        assert np.max(np.abs(w - scipy.special.softmax(s))) <= 1e-15
+        assert abs(m + math.log(l) - scipy.special.logsumexp(s)) <= 1e-13
+
+
+# ---------------------------------------------------------------- T3 ----
+@pytest.mark.parametrize("causal", [False, True])
+def test_weights_sum_to_one_and_match_library(causal):
+    rng = np.random.default_rng(3)
+    q, k = _rand(rng, 33, 16), _rand(rng, 33, 16)
+    w = orc.attention_weights(q, k, 0.25, causal)
+    assert np.max(np.abs(w.sum(axis=1) - 1.0)) <= 1e-12
+    s = 0.25 * (q @ k.T)
+    if causal:
+        s = np.where(np.tril(np.ones((33, 33), dtype=bool)), s, -np.inf)
+    assert np.max(np.abs(w - scipy.special.softmax(s, axis=1))) <= 1e-15
+    _, lse = orc.attention_definition(q, k, np.eye(33), 0.25, causal)
+    assert np.max(np.abs(lse - scipy.special.logsumexp(s, axis=1))) <= 1e-13
+
+
+# ---------------------------------------------------------------- T4 ----
+def test_joint_kv_permutation_invariance():
+    rng = np.random.default_rng(4)
+    q, k, v = _rand(rng, 20, 8), _rand(rng, 50, 8), _rand(rng, 50, 8)
+    perm = rng.permutation(50)
+    o1, l1 = orc.attention_definition(q, k, v, 0.3, False)
+    o2, l2 = orc.attention_definition(q, k[perm], v[perm], 0.3, False)
+    assert np.max(np.abs(o1 - o2)) <= 1e-12
+    assert np.max(np.abs(l1 - l2)) <= 1e-12
+
+
+# ---------------------------------------------------------------- T5 ----
+def test_causal_row0_is_v0_and_varlen_first_tokens():
+    rng = np.random.default_rng(5)
+    q, k, v = _rand(rng, 9, 4), _rand(rng, 9, 4), _rand(rng, 9, 4)
+    o, lse = orc.attention_definition(q, k, v, 1.0, True)
+    assert np.array_equal(o[0], v[0])
+    assert lse[0] == pytest.approx(float(q[0] @ k[0]), abs=1e-15)
+    # varlen: the first token of every packed sequence sees only itself
+    lens = [3, 1, 5]
+    cu = np.cumsum([0] + lens)
+    T = cu[-1]
+    qv, kv, vv = _rand(rng, T, 2, 4), _rand(rng, T, 2, 4), _rand(rng, T, 2, 4)
+    ov, _ = orc.attn_fwd(qv, kv, vv, 0.5, True, cu_seqlens=cu)
+    for a in cu[:-1]:
+        assert np.array_equal(ov[a], vv[a])
+
+
+# ---------------------------------------------------------------- T6 ----
+def test_uniform_weights_closed_form():
+    """K = 0 makes every score equal: O = mean(V) (causal: prefix means)."""
+    rng = np.random.default_rng(6)
+    q, v = _rand(rng, 12, 8), _rand(rng, 12, 5)
+    k = np.zeros((12, 8))
+    o, lse = orc.attention_definition(q, k, v, 1.0, False)
+    assert np.max(np.abs(o - v.mean(axis=0))) <= 1e-14
+    assert np.max(np.abs(lse - math.log(12))) <= 1e-14
+    o, lse = orc.attention_definition(q, k, v, 1.0, True)
+    prefix = np.cumsum(v, axis=0) / np.arange(1, 13)[:, None]
+    assert np.max(np.abs(o - prefix)) <= 1e-14
+    assert np.max(np.abs(lse - np.log(np.arange(1, 13)))) <= 1e-14
+
+
+def test_dominant_score_and_no_overflow():
+    """One score far above the rest picks its value row; huge scores stay finite."""
+    d = 4
+    q = np.array([[1.0, 0, 0, 0]])
+    s = np.array([3.0, -1.0, 1000.0, 2.0])          # gap >= 200 at index 2
+    k = np.zeros((4, d))
+    k[:, 0] = s
+    v = np.arange(16, dtype=float).reshape(4, 4)
+    o, lse = orc.attention_definition(q, k, v, 1.0, False)
+    assert np.array_equal(o[0], v[2])               # other weights underflow to 0
+    assert lse[0] == 1000.0
+    # e^{1000} overflows fp64 without the max subtraction
+    for bs in (1, 2, 3):
+        ob, lb = orc.attention_blocked(q, k, v, 1.0, False, bs)
+        assert np.all(np.isfinite(ob)) and np.array_equal(ob[0], v[2]) and lb[0] == 1000.0
+
+
+# ---------------------------------------------------------------- T7 ----
+@pytest.mark.parametrize("seed", range(5))
+def test_merge_of_split_partials_equals_unsplit(seed):
+    """'Flash-Decoding': partials over chunks of K/V merged by the same rule."""
+    rng = np.random.default_rng(100 + seed)
+    nk, d = 61, 16
+    q, k, v = _rand(rng, 3, d), _rand(rng, nk, d), _rand(rng, nk, d)
+    o_ref, lse_ref = orc.attention_definition(q, k, v, 0.4, False)
+    n_cuts = int(rng.integers(1, 8))
+    cuts = sorted(set(rng.integers(1, nk, n_cuts).tolist()))
+    bounds = [0] + cuts + [nk]
+    lp, op = [], []
+    for a, e in zip(bounds[:-1], bounds[1:]):
+        o_s, l_s = orc.attention_definition(q, k[a:e], v[a:e], 0.4, False)
+        lp.append(l_s)
+        op.append(o_s)
+    lp.append(np.full(3, -np.inf))                  # an empty split
+    op.append(np.full((3, d), np.nan))              # never read
+    lse_part = np.stack(lp, axis=-1)
+    o_part = np.stack(op, axis=1)
+    o, lse = orc.merge_partials(lse_part, o_part)
+    assert np.max(np.abs(o - o_ref)) <= 1e-12
+    assert np.max(np.abs(lse - lse_ref)) <= 1e-12
+
+
+def test_merge_all_empty_is_zero_and_minus_inf():
+    o, lse = orc.merge_partials(np.full((2, 4), -np.inf), np.ones((2, 4, 3)))
+    assert np.array_equal(o, np.zeros((2, 3)))
+    assert np.all(lse == -np.inf)
+
+
+# ---------------------------------------------------------------- GQA / varlen ----
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    rng = np.random.default_rng(8)
+    B, N, Hq, Hkv, d = 2, 9, 6, 2, 4
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    o, lse = orc.attn_fwd(q, k, v, 0.5, True)
+    kr, vr = np.repeat(k, Hq // Hkv, axis=2), np.repeat(v, Hq // Hkv, axis=2)
+    for h in range(Hq):
+        assert np.array_equal(kr[:, :, h], k[:, :, h // 3])
+    o2, lse2 = orc.attn_fwd(q, kr, vr, 0.5, True)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_varlen_has_no_cross_sequence_attention():
+    rng = np.random.default_rng(9)
+    lens = [4, 7, 1, 5]
+    cu = np.cumsum([0] + lens)
+    T, H, d = cu[-1], 2, 4
+    q, k, v = _rand(rng, T, H, d), _rand(rng, T, H, d), _rand(rng, T, H, d)
+    o, lse = orc.attn_fwd(q, k, v, 0.5, True, cu_seqlens=cu)
+    for b, (a, e) in enumerate(zip(cu[:-1], cu[1:])):
+        for h in range(H):
+            o_ref, l_ref = _python_attention(q[a:e, h].tolist(), k[a:e, h].tolist(),
+                                             v[a:e, h].tolist(), 0.5, True)
+            assert np.max(np.abs(o[a:e, h] - o_ref)) <= 1e-13
+            assert np.max(np.abs(lse[h, a:e] - l_ref)) <= 1e-13
+
+
+def test_sampled_rows_match_full_output():
+    rng = np.random.default_rng(10)
+    q, k, v = _rand(rng, 2, 11, 4, 8), _rand(rng, 2, 11, 2, 8), _rand(rng, 2, 11, 2, 8)
+    o, lse = orc.attn_fwd(q, k, v, 0.3, True)
+    samples = np.array([[0, 0, 0], [1, 3, 10], [0, 2, 5], [1, 1, 7]])
+    os_, ls_ = orc.attn_fwd_rows(q, k, v, 0.3, True, samples)
+    for n, (b, h, i) in enumerate(samples):
+        assert np.max(np.abs(os_[n] - o[b, i, h])) <= 1e-14 and abs(ls_[n] - lse[b, h, i]) <= 1e-14
+
+
+# ---------------------------------------------------------------- paged decode ----
+def _small_paged(rng, lens, page_size, Hkv, d, spare=3):
+    pages = [-(-n // page_size) for n in lens]
+    pool = sum(pages) + spare
+    perm = rng.permutation(pool)
+    max_pages = max(pages) + 2
+    table = np.zeros((len(lens), max_pages), dtype=np.int32)
+    kc = np.full((pool, page_size, Hkv, d), 1e4)
+    vc = np.full((pool, page_size, Hkv, d), 1e4)
+    k_log, v_log = [], []
+    off = 0
+    for b, n in enumerate(lens):
+        table[b, : pages[b]] = perm[off: off + pages[b]]
+        table[b, pages[b]:] = perm[-1]                       # a spare page
+        kl, vl = _rand(rng, n, Hkv, d), _rand(rng, n, Hkv, d)
+        for t in range(n):                                   # scatter token by token
+            kc[table[b, t // page_size], t % page_size] = kl[t]
+            vc[table[b, t // page_size], t % page_size] = vl[t]
+        k_log.append(kl)
+        v_log.append(vl)
+        off += pages[b]
+    return kc, vc, table, k_log, v_log
+
+
+def test_paged_gather_is_bit_exact():
+    rng = np.random.default_rng(11)
+    lens = [1, 16, 17, 40]
+    kc, vc, table, k_log, _ = _small_paged(rng, lens, 16, 2, 4)
+    for b, n in enumerate(lens):
+        assert np.array_equal(orc.gather_paged(kc, table, b, n), k_log[b])
+
+
+def test_paged_decode_equals_contiguous_definition():
+    rng = np.random.default_rng(12)
+    lens = [5, 33, 64, 1]
+    Hq, Hkv, d = 4, 2, 8
+    kc, vc, table, k_log, v_log = _small_paged(rng, lens, 16, Hkv, d)
+    q = _rand(rng, len(lens), Hq, d)
+    o, lse = orc.decode_paged(q, kc, vc, table, lens, 0.35)
+    for b, n in enumerate(lens):
+        for h in range(Hq):
+            o_ref, l_ref = _python_attention([q[b, h].tolist()], k_log[b][:, h // 2].tolist(),
+                                             v_log[b][:, h // 2].tolist(), 0.35, False)
+            assert np.max(np.abs(o[b, h] - o_ref[0])) <= 1e-13
+            assert abs(lse[b, h] - l_ref[0]) <= 1e-13
+
+
+def test_split_ranges_partition_each_sequence():
+    lens = [1, 15, 16, 17, 100, 257, 0]
+    for ps in (1, 16, 32):
+        for max_pages in (-(-257 // ps), -(-257 // ps) + 5):
+            for S in (1, 2, 3, 7, 16, 64, 400):
+                r = orc.decode_split_ranges(lens, ps, max_pages, S)
+                C = -(-max_pages // S)
+                for b, n in enumerate(lens):
+                    covered = []
+                    for s in range(S):
+                        a, e = r[b, s]
+                        assert 0 <= a <= e <= n
+                        assert e - a <= C * ps
+                        if e > a:
+                            assert a == s * C * ps           # whole pages, in order
+                            covered.extend(range(a, e))
+                    assert covered == list(range(n))
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 16])
+def test_decode_partials_merge_to_decode(S):
+    rng = np.random.default_rng(13)
+    lens = [5, 33, 64, 1, 47]
+    Hq, Hkv, d = 4, 1, 8
+    kc, vc, table, _, _ = _small_paged(rng, lens, 16, Hkv, d)
+    q = _rand(rng, len(lens), Hq, d)
+    o_ref, lse_ref = orc.decode_paged(q, kc, vc, table, lens, 0.35)
+    lp, op = orc.decode_partials(q, kc, vc, table, lens, 0.35, S)
+    o, lse = orc.merge_partials(lp, op)
+    assert np.max(np.abs(o - o_ref)) <= 1e-12
+    assert np.max(np.abs(lse - lse_ref)) <= 1e-12
