@@ -1,0 +1,366 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on one GB300 (replicas on N GPUs).
+
+One step = one pass of the whole path on one synthetic batch:
+  * prefill: causal MHA, B=4, Hq=Hkv=32, N=4096, d=128, bf16 (tensor-core kernel);
+  * decode: paged split-KV, batch 8, Hq=32, Hkv=8, d=128, contexts U[1024, 65536]
+    (seed 4), 16-token pages (decode-partials kernel + merge kernel).
+``value`` is prefill causal-adjusted TFLOP/s (4*B*Hq*N^2*d / 2 per step) summed
+over ranks; decode KV GB/s is reported beside it. Inputs are resident in HBM
+when timing starts; L2 is flushed (256 MB write) before every timed launch.
+``e2e`` repeats the step through the same public API from pinned host buffers,
+host<->device copies included.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same prefill workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill attention TFLOP/s & decode KV GB/s, % of GB300 roofline (1 GPU)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--num-splits", type=int, default=0, help="decode splits (0 = library heuristic)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        # samples under load: the upper half by power
+        thr = sorted(power)[len(power) // 2] if power else 0
+        loaded = [s for s, p in zip(sm, power) if p >= thr] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- workloads
+def make_workloads():
+    from exact_tiled_attention_fattn_gb300 import inputs
+    pre = inputs.causal_mha_config()
+    dec = inputs.paged_decode_config()
+    return pre, dec
+
+
+def cpu_baseline_prefill(pre, seconds: float):
+    """Time the fp64 oracle on sampled query rows of the prefill workload."""
+    import numpy as np
+    from oracle import attention as orc
+    B, N, Hq, d = pre.q.shape
+    rng = np.random.default_rng(0)
+    done_rows, flops, t_used = 0, 0.0, 0.0
+    chunk = 64
+    heads = 0
+    while t_used < seconds:
+        b, h = int(rng.integers(B)), int(rng.integers(Hq))
+        rows = np.sort(rng.choice(N, size=chunk, replace=False))
+        smp = np.stack([np.full(chunk, b), np.full(chunk, h), rows], axis=1)
+        t0 = time.perf_counter()
+        orc.attn_fwd_rows(pre.q, pre.k, pre.v, pre.scale, True, smp)
+        t_used += time.perf_counter() - t0
+        flops += float(np.sum(4.0 * d * (rows + 1)))      # causal: row i sees i+1 keys
+        done_rows += chunk
+        heads += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / t_used / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done_rows} query rows ({heads} random (b, head) pairs x {chunk} rows) of the "
+                      f"B=4 H=32 N=4096 d=128 causal prefill, fp64 numpy (BLAS threads = cores), "
+                      f"{t_used:.1f} s"}
+
+
+def run_reference(args):
+    """The oracle as it stands, on host cores, on bounded samples of the prefill workload."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    pre, _ = make_workloads()
+    per_step = max(1.0, min(6.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline_prefill(pre, per_step / 4)
+    vals = [cpu_baseline_prefill(pre, per_step) for _ in range(args.steps)]
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "ms_per_step": per_step * 1e3,
+            "config": {"workload": "causal MHA prefill B=4 Hq=Hkv=32 N=4096 d=128 (oracle on sampled rows)",
+                       "l2": "n/a (host)"},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    import torch
+    import torch.distributed as dist
+    from exact_tiled_attention_fattn_gb300 import build, fattn
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    build.build()
+    fattn.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+
+    pre, dec = make_workloads()
+    q, k, v = pre.q.to(dev), pre.k.to(dev), pre.v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty((pre.q.shape[0], pre.hq, pre.q.shape[1]), dtype=torch.float32, device=dev)
+    dq, dk, dv = dec.q.to(dev), dec.kcache.to(dev), dec.vcache.to(dev)
+    dbt, dsl = dec.block_table.to(dev), dec.seqlens.to(dev)
+    S = args.num_splits or fattn.choose_num_splits(dec.batch, dec.hkv, dec.max_pages_per_seq)
+    ws = torch.empty(fattn.decode_workspace_size(dec.batch, dec.hq, dec.d, S), dtype=torch.uint8, device=dev)
+    do = torch.empty_like(dq)
+    dlse = torch.empty((dec.batch, dec.hq), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def prefill():
+        fattn.fwd(q, k, v, causal=True, scale=pre.scale, out=o, lse=lse)
+
+    def decode():
+        fattn.decode_paged(dq, dk, dv, dbt, dsl, S, scale=dec.scale, out=do, lse=dlse, workspace=ws)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        prefill()
+        flush.zero_()
+        decode()
+    torch.cuda.synchronize()
+    assert fattn.debug_read_status() == 0
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        prefill()
+        ev[s][1].record(stream)
+        flush.zero_()
+        ev[s][2].record(stream)
+        decode()
+        ev[s][3].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clocks = sampler.stop()
+    launches = 3 * args.steps
+    status = fattn.debug_read_status()
+
+    pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
+    t_pre = sum(pre_ms) / len(pre_ms)
+    t_dec = sum(dec_ms) / len(dec_ms)
+    if world > 1:
+        tt = torch.tensor([t_pre, t_dec], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_pre, t_dec = tt.tolist()
+
+    flops = pre.flops()
+    kv_bytes = dec.kv_bytes()
+    tflops = flops / (t_pre * 1e-3) / 1e12
+    gbs = kv_bytes / (t_dec * 1e-3) / 1e9
+    peaks, peak_src = load_peaks()
+
+    # ---------------------------------------------------------------- e2e through host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq_, hk_, hv_ = pre.q.pin_memory(), pre.k.pin_memory(), pre.v.pin_memory()
+        ho = torch.empty_like(pre.q).pin_memory()
+        hl = torch.empty(lse.shape, dtype=torch.float32).pin_memory()
+        hdq, hdk, hdv = dec.q.pin_memory(), dec.kcache.pin_memory(), dec.vcache.pin_memory()
+        hbt, hsl = dec.block_table.pin_memory(), dec.seqlens.pin_memory()
+        hdo = torch.empty_like(dec.q).pin_memory()
+        hdl = torch.empty((dec.batch, dec.hq), dtype=torch.float32).pin_memory()
+        h2d_pre = sum(t.numel() * t.element_size() for t in (hq_, hk_, hv_))
+        d2h_pre = ho.numel() * ho.element_size() + hl.numel() * 4
+        h2d_dec = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv, hbt, hsl))
+        d2h_dec = hdo.numel() * hdo.element_size() + hdl.numel() * 4
+
+        def e2e_prefill():
+            q.copy_(hq_, non_blocking=True)
+            k.copy_(hk_, non_blocking=True)
+            v.copy_(hv_, non_blocking=True)
+            prefill()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+
+        def e2e_decode():
+            dq.copy_(hdq, non_blocking=True)
+            dk.copy_(hdk, non_blocking=True)
+            dv.copy_(hdv, non_blocking=True)
+            dbt.copy_(hbt, non_blocking=True)
+            dsl.copy_(hsl, non_blocking=True)
+            decode()
+            hdo.copy_(do, non_blocking=True)
+            hdl.copy_(dlse, non_blocking=True)
+
+        for _ in range(2):
+            e2e_prefill()
+            e2e_decode()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 10))
+        ee = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n_e2e)]
+        for s in range(n_e2e):
+            ee[s][0].record(stream)
+            e2e_prefill()
+            ee[s][1].record(stream)
+            e2e_decode()
+            ee[s][2].record(stream)
+        torch.cuda.synchronize()
+        tp = sum(e[0].elapsed_time(e[1]) for e in ee) / n_e2e
+        td = sum(e[1].elapsed_time(e[2]) for e in ee) / n_e2e
+        if world > 1:
+            tt = torch.tensor([tp, td], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            tp, td = tt.tolist()
+        e2e = {"value": world * flops / (tp * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d_pre + h2d_dec, "d2h_bytes_per_step": d2h_pre + d2h_dec,
+               "prefill_ms": tp, "decode_ms": td,
+               "decode": {"value": world * kv_bytes / (td * 1e-3) / 1e9, "unit": "GB/s"}}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_prefill(pre, args.cpu_seconds)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    peak_t = peaks["bf16_tflops"]
+    peak_b = peaks["hbm_gbs"]
+    line = {
+        "metric": METRIC,
+        "value": world * tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t_pre + t_dec,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "causal MHA prefill B=4 Hq=Hkv=32 N=4096 d=128 + paged split-KV decode "
+                               "B=8 Hq=32 Hkv=8 d=128 ctx U[1024,65536] seed 4, 16-token pages",
+                   "parallelism": f"replicas x{world}", "num_splits": S,
+                   "l2": "flushed (256 MB write) before every timed launch"},
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
+                     "frac": tflops / peak_t, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)", "kernel": "prefill_tc_kernel<128>"},
+        "decode": {"value": world * gbs, "unit": "GB/s", "ms": t_dec, "kv_bytes": kv_bytes,
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_b, "unit": "GB/s",
+                                "frac": gbs / peak_b, "traffic": None, "peak_source": f"{peak_src} hbm_gbs"}},
+        "prefill_ms": t_pre,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "clocks": clocks,
+        "gpu_launches": launches,
+        "device_status": status,
+        "wall_s_timed": t_wall,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+// libfattn C ABI: argument validation, the device status word, TMA
+// descriptor encoding and kernel dispatch. See include/fattn.h for the
+// contract of every entry point.
+#include "fattn.h"
+#include "fattn_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+namespace fattn {
+
+// First device-side problem since the last fattn_debug_read_status().
+__device__ int g_status_word = 0;
+
+static std::atomic<int*> g_status_ptr[128];
+
+int* status_ptr(int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
+    *err = 1;
+    return nullptr;
+  }
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (p) return p;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess || addr == nullptr) {
+    *err = 1;
+    return nullptr;
+  }
+  g_status_ptr[dev].store(static_cast<int*>(addr), std::memory_order_release);
+  return static_cast<int*>(addr);
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 3-D bf16 view [rows, H, d] (d innermost) with a box of box_rows x 1 head x
+// 64 elements (128 bytes, the 128-byte swizzle span). Rows past `rows` read as
+// zero.
+bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int H, int d, int box_rows) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms_current() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+}  // namespace fattn
+
+using namespace fattn;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+extern "C" const char* fattn_status_string(fattn_status s) {
+  switch (s) {
+    case FATTN_OK: return "ok";
+    case FATTN_ERR_INVALID_ARG: return "invalid argument";
+    case FATTN_ERR_UNSUPPORTED: return "unsupported configuration";
+    case FATTN_ERR_WORKSPACE: return "workspace missing or too small";
+    case FATTN_ERR_CUDA: return "CUDA error";
+    case FATTN_ERR_TIMEOUT: return "device pipeline wait timed out";
+    case FATTN_ERR_DEVICE_CHECK: return "device-side index check failed";
+  }
+  return "unknown status";
+}
+
+extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                  int Hkv, int N, int d, int causal, float scale, const int32_t* cu_seqlens,
+                                  int total_tokens, fattn_dtype dtype, cudaStream_t stream) {
+  if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || total_tokens < 0) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (dtype != FATTN_BF16 && dtype != FATTN_FP32) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = cu_seqlens ? (long long)total_tokens : (long long)B * N;
+  if (B == 0 || N == 0 || rows == 0) return FATTN_OK;
+  if (rows > 0x7fffffffLL || (long long)B * Hq * N > 0x7fffffffLL * 4LL) return FATTN_ERR_UNSUPPORTED;
+
+  int err = 0;
+  PrefillParams p;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = cu_seqlens;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
+  p.causal = causal ? 1 : 0; p.scale = scale;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+
+  cudaError_t e;
+  if (dtype == FATTN_FP32) {
+    e = launch_prefill_f32(p, stream);
+  } else {
+    CUtensorMap tq, tk, tv;
+    if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
+        !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+      return FATTN_ERR_CUDA;
+    int sms = num_sms_current();
+    if (sms <= 0) return FATTN_ERR_CUDA;
+    e = launch_prefill_tc(p, tq, tk, tv, sms, stream);
+  }
+  return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+extern "C" size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
+  if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
+  size_t rows = (size_t)B * Hq * num_splits;
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+}
+
+extern "C" fattn_status fattn_decode_paged(const void* q, const void* kcache, const void* vcache,
+                                           const int32_t* block_table, const int32_t* seqlens, int num_splits,
+                                           void* o, float* lse, int B, int Hq, int Hkv, int d, int page_size,
+                                           int max_pages_per_seq, int num_pages, float scale, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !kcache || !vcache || !block_table || !seqlens || !o) return FATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || page_size <= 0 || max_pages_per_seq <= 0 || num_pages <= 0 ||
+      num_splits <= 0)
+    return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return FATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens) & 3u))
+    return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)num_pages * page_size * Hkv * d > (1LL << 40)) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * num_splits > 0x7fffffffLL / 512) return FATTN_ERR_UNSUPPORTED;
+  const size_t need = fattn_decode_workspace_size(B, Hq, d, num_splits);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FATTN_ERR_WORKSPACE;
+
+  int err = 0;
+  DecodeParams p;
+  p.q = q; p.kcache = kcache; p.vcache = vcache; p.block_table = block_table; p.seqlens = seqlens;
+  const size_t rows = (size_t)B * Hq * num_splits;
+  p.lse_part = static_cast<float*>(workspace);
+  p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)));
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.page_size = page_size; p.max_pages_per_seq = max_pages_per_seq;
+  p.num_pages = num_pages; p.num_splits = num_splits; p.scale = scale;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  if (launch_decode_partials(p, stream) != cudaSuccess) return FATTN_ERR_CUDA;
+
+  MergeParams m;
+  m.o_part = p.o_part; m.lse_part = p.lse_part; m.o = o; m.lse = lse;
+  m.B = B; m.Hq = Hq; m.S = num_splits; m.d = d; m.out_bf16 = 1;
+  return launch_merge(m, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+extern "C" fattn_status fattn_merge_partials(const float* o_part, const float* lse_part, void* o, float* lse, int B,
+                                             int Hq, int num_splits, int d, fattn_dtype out_dtype,
+                                             cudaStream_t stream) {
+  if (!o_part || !lse_part || !o) return FATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || num_splits <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
+  if (out_dtype != FATTN_BF16 && out_dtype != FATTN_FP32) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(o_part) || !aligned16(o) || (reinterpret_cast<uintptr_t>(lse_part) & 3u))
+    return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (d % 4 != 0 || d > 512) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq * num_splits * d > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+  MergeParams m;
+  m.o_part = o_part; m.lse_part = lse_part; m.o = o; m.lse = lse;
+  m.B = B; m.Hq = Hq; m.S = num_splits; m.d = d; m.out_bf16 = out_dtype == FATTN_BF16;
+  return launch_merge(m, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+extern "C" fattn_status fattn_debug_read_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FATTN_ERR_CUDA;
+  int err = 0;
+  int* p = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  int h = 0, zero = 0;
+  if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FATTN_ERR_CUDA;
+  return static_cast<fattn_status>(h);
+}

@@ -1,0 +1,64 @@
+// Internal launchers of libfattn (not part of the ABI). Each returns a
+// cudaError_t from the launch; argument checks happen in api.cu before these
+// are called.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fattn {
+
+// Device status word codes (match fattn_status).
+enum : int { kStatusOk = 0, kStatusTimeout = 5, kStatusDeviceCheck = 6 };
+
+// Problem description shared by both prefill kernels.
+struct PrefillParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  const int32_t* cu_seqlens;  // device; nullptr = dense
+  int B, Hq, Hkv, N, d;       // N = sequence length (dense) / max length (varlen)
+  int total_rows;             // rows of the packed [rows, H, d] view (B*N or T)
+  int causal;
+  float scale;
+  int* status;                // device status word
+};
+
+// Tensor-core prefill (bf16 in, fp32 accumulate, bf16 out). Tensor maps are
+// encoded by the caller over the packed [rows, H, d] views of q, k and v.
+cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
+                              const CUtensorMap& tv, int num_sms, cudaStream_t stream);
+
+// CUDA-core fp32 prefill.
+cudaError_t launch_prefill_f32(const PrefillParams& p, cudaStream_t stream);
+
+struct DecodeParams {
+  const void* q;
+  const void* kcache;
+  const void* vcache;
+  const int32_t* block_table;
+  const int32_t* seqlens;
+  float* lse_part;  // [B, Hq, S]
+  float* o_part;    // [B, Hq, S, d]
+  int B, Hq, Hkv, d, page_size, max_pages_per_seq, num_pages, num_splits;
+  float scale;
+  int* status;
+};
+
+cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
+
+struct MergeParams {
+  const float* o_part;
+  const float* lse_part;
+  void* o;
+  float* lse;
+  int B, Hq, S, d;
+  int out_bf16;
+};
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+
+}  // namespace fattn

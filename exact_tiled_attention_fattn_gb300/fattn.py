@@ -1,0 +1,215 @@
+"""Thin Python binding of libfattn (ctypes): argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels; this module
+checks tensor shapes/dtypes, allocates outputs with PyTorch when the caller
+does not pass them, and forwards raw device pointers and the current CUDA
+stream. There is no fallback: if ``libfattn.so`` is missing or fails to load,
+every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libfattn.so")
+
+FATTN_OK = 0
+FATTN_ERR_INVALID_ARG = 1
+FATTN_ERR_UNSUPPORTED = 2
+FATTN_ERR_WORKSPACE = 3
+FATTN_ERR_CUDA = 4
+FATTN_ERR_TIMEOUT = 5
+FATTN_ERR_DEVICE_CHECK = 6
+FATTN_BF16 = 0
+FATTN_FP32 = 1
+
+# Every entry point declared in include/fattn.h: name -> (restype, argtypes)
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "fattn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _i, _vp]),
+    "fattn_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "fattn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz,
+                                _vp]),
+    "fattn_merge_partials": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
+    "fattn_status_string": (ctypes.c_char_p, [_i]),
+    "fattn_debug_read_status": (_i, [_vp]),
+}
+
+_lib = None
+
+
+class FattnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} (status {status})")
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libfattn.so and declare its C signatures; raises if it is absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"libfattn.so not found at {path}: build it with __graft_entry__.build() "
+                           "or python -m exact_tiled_attention_fattn_gb300.build")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().fattn_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != FATTN_OK:
+        raise FattnError(fn, status)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(dt) -> int:
+    if dt == torch.bfloat16:
+        return FATTN_BF16
+    if dt == torch.float32:
+        return FATTN_FP32
+    raise TypeError(f"unsupported dtype {dt}: bf16 or fp32 only")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+
+
+def fwd(q, k, v, causal: bool = False, scale: float | None = None, cu_seqlens=None, max_seqlen: int | None = None,
+        out=None, lse=None, want_lse: bool = True, stream=None):
+    """Prefill attention. Dense q [B,N,Hq,d] / k,v [B,N,Hkv,d]; varlen q [T,Hq,d] with
+    int32 ``cu_seqlens`` [B+1] on the device and ``max_seqlen`` (host int).
+    Returns (O, lse): lse is [B,Hq,N] (dense) or [Hq,T] (varlen), fp32, natural log.
+    """
+    lib = load_library()
+    _need_cuda(q, k, v, cu_seqlens, out, lse)
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k and v must share a dtype")
+    d = q.shape[-1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if cu_seqlens is None:
+        if q.dim() != 4:
+            raise ValueError("dense q must be [B, N, Hq, d]")
+        B, N, Hq, _ = q.shape
+        Hkv = k.shape[2]
+        T = B * N
+        lse_shape = (B, Hq, N)
+    else:
+        if q.dim() != 3 or max_seqlen is None:
+            raise ValueError("varlen q must be [T, Hq, d] and max_seqlen must be given")
+        if cu_seqlens.dtype != torch.int32:
+            raise TypeError("cu_seqlens must be int32")
+        T, Hq, _ = q.shape
+        Hkv = k.shape[1]
+        B = cu_seqlens.numel() - 1
+        N = int(max_seqlen)
+        lse_shape = (Hq, T)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(lse_shape, dtype=torch.float32, device=q.device)
+    st = lib.fattn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, 1 if causal else 0,
+                       float(scale), _ptr(cu_seqlens), T if cu_seqlens is not None else 0, _dtype_code(q.dtype),
+                       ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_fwd", st)
+    return out, lse
+
+
+def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
+    return int(load_library().fattn_decode_workspace_size(B, Hq, d, num_splits))
+
+
+def choose_num_splits(batch: int, hkv: int, max_pages_per_seq: int, num_sms: int | None = None,
+                      chunk_pages: int = 32) -> int:
+    """A split count that cuts contexts into ~``chunk_pages``-page chunks and gives at
+    least two thread blocks per SM over the batch."""
+    if num_sms is None:
+        num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    by_chunk = -(-max_pages_per_seq // chunk_pages)
+    by_fill = -(-2 * num_sms // max(1, batch * hkv))
+    return max(1, min(max_pages_per_seq, max(by_chunk, by_fill)))
+
+
+def decode_paged(q, kcache, vcache, block_table, seqlens, num_splits: int, scale: float | None = None,
+                 out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """Split-KV paged decode. q [B,Hq,d] bf16; kcache/vcache [pages, page_size, Hkv, d] bf16;
+    block_table int32 [B, max_pages_per_seq]; seqlens int32 [B]. Returns (O [B,Hq,d], lse [B,Hq])."""
+    lib = load_library()
+    _need_cuda(q, kcache, vcache, block_table, seqlens, out, lse, workspace)
+    if block_table.dtype != torch.int32 or seqlens.dtype != torch.int32:
+        raise TypeError("block_table and seqlens must be int32")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = kcache.shape
+    maxp = block_table.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    need = decode_workspace_size(B, Hq, d, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.fattn_decode_paged(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table), _ptr(seqlens), num_splits,
+                                _ptr(out), _ptr(lse), B, Hq, Hkv, d, page_size, maxp, num_pages, float(scale),
+                                _ptr(workspace), ws_bytes, ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_decode_paged", st)
+    return out, lse
+
+
+def split_workspace(workspace, B: int, Hq: int, d: int, num_splits: int):
+    """Views (lse_part [B,Hq,S], o_part [B,Hq,S,d]) of a decode workspace (fp32)."""
+    rows = B * Hq * num_splits
+    lse_bytes = (rows * 4 + 255) // 256 * 256
+    flat = workspace.view(torch.uint8)
+    lse_part = flat[: rows * 4].view(torch.float32).view(B, Hq, num_splits)
+    o_part = flat[lse_bytes: lse_bytes + rows * d * 4].view(torch.float32).view(B, Hq, num_splits, d)
+    return lse_part, o_part
+
+
+def merge_partials(o_part, lse_part, out_dtype=torch.bfloat16, out=None, lse=None, want_lse: bool = True,
+                   stream=None):
+    """Merge split partials: o_part [B,Hq,S,d] fp32, lse_part [B,Hq,S] fp32 -> (O [B,Hq,d], lse [B,Hq])."""
+    lib = load_library()
+    _need_cuda(o_part, lse_part, out, lse)
+    B, Hq, S, d = o_part.shape
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=out_dtype, device=o_part.device)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=o_part.device)
+    st = lib.fattn_merge_partials(_ptr(o_part), _ptr(lse_part), _ptr(out), _ptr(lse), B, Hq, S, d,
+                                  _dtype_code(out.dtype), ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_merge_partials", st)
+    return out, lse
+
+
+def debug_read_status(stream=None) -> int:
+    """Synchronise the stream, then read and clear the device status word."""
+    return int(load_library().fattn_debug_read_status(ctypes.c_void_p(_stream_handle(stream))))

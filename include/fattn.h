@@ -1,0 +1,168 @@
+/*
+ * fattn.h — C ABI of libfattn: exact tiled attention on GB300 (sm_103a).
+ *
+ * The library computes exact attention, O = softmax(Q K^T * scale + M) V, tile
+ * by tile with the online-softmax (m, l, O) rescaling rule, so the N x N score
+ * and probability matrices never reach device memory. Sources:
+ *   [FA-LLM]   "FlashAttention" (LLM-inference guide, ch. 10): the formula;
+ *              "The trick: tiles and an online softmax" (update rule);
+ *              "Decode is a different problem" / "Flash-Decoding" (split-K
+ *              partials merged with the same rule); family table rows
+ *              "Flash-Decoding" and "Paged variants".
+ *   [FA-PAPER] "FlashAttention, explained": "The forward pass" steps 1-5
+ *              (inputs Q, K, V of N x d per head in device memory, scale and
+ *              mask fused, output O plus the per-row statistics l and m).
+ *   [CUDA-OPS] "Attention" CUDA operations guide: K/V heads shared by several
+ *              Q heads; non-contiguous (paged) KV allocation.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers, owned by the caller, row-major,
+ *     densely packed in the layout stated per call, and 16-byte aligned. The
+ *     library never allocates, frees or synchronises on these calls.
+ *   - Every call validates its arguments on the host first. On failure it
+ *     returns a status and launches nothing; no call aborts or throws.
+ *   - Work is enqueued on `stream` (0 = legacy default stream). A launch
+ *     failure returns FATTN_ERR_CUDA. Problems found on the device (a
+ *     block-table entry outside the pool, a sequence longer than its table,
+ *     inconsistent cu_seqlens, a pipeline wait that did not finish within its
+ *     time limit) are recorded in a device status word and the offending work
+ *     is skipped; fattn_debug_read_status() reads and clears that word.
+ *   - Query head h reads KV head h / (Hq / Hkv) (GQA; MQA when Hkv = 1).
+ *   - lse is the natural-log logsumexp of the scaled, masked scores of a row,
+ *     lse = m + ln(l); a row with no visible key has O = 0, lse = -inf.
+ *   - Supported head dimensions: d = 64 and d = 128.
+ */
+#ifndef FATTN_H
+#define FATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FATTN_OK = 0,
+  FATTN_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad size, Hq % Hkv != 0 */
+  FATTN_ERR_UNSUPPORTED = 2,   /* valid request outside the supported set (e.g. d = 96) */
+  FATTN_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required */
+  FATTN_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  FATTN_ERR_TIMEOUT = 5,       /* device status: a bounded pipeline wait expired */
+  FATTN_ERR_DEVICE_CHECK = 6   /* device status: an index check failed, work skipped */
+} fattn_status;
+
+typedef enum {
+  FATTN_BF16 = 0,
+  FATTN_FP32 = 1
+} fattn_dtype;
+
+/*
+ * fattn_fwd — prefill: exact attention for all query rows of a batch.
+ * [FA-PAPER] "The forward pass"; [FA-LLM] formula and "The trick".
+ *
+ * Dense (cu_seqlens == NULL): q [B, N, Hq, d], k and v [B, N, Hkv, d],
+ *   o [B, N, Hq, d] (same dtype as q), lse [B, Hq, N] fp32.
+ * Varlen (cu_seqlens != NULL): B sequences packed back to back;
+ *   cu_seqlens is a DEVICE int32 array [B + 1] with cu_seqlens[0] = 0,
+ *   non-decreasing, cu_seqlens[B] = total_tokens; q [T, Hq, d], k and v
+ *   [T, Hkv, d], o [T, Hq, d], lse [Hq, T] with T = total_tokens; N must be
+ *   >= every sequence length (it sizes the launch; the host never reads
+ *   cu_seqlens). No attention crosses a sequence boundary.
+ * causal != 0 applies M = -inf above the diagonal of each sequence
+ *   (key j visible to query i iff j <= i).
+ * scale multiplies Q K^T (1/sqrt(d) is the usual choice); must be finite.
+ * dtype: FATTN_BF16 runs the tensor-core kernel (fp32 accumulation, P rounded
+ *   to bf16 for the P V product, O rounded to nearest even); FATTN_FP32 runs
+ *   the CUDA-core fp32 kernel (inputs and outputs fp32).
+ * lse may be NULL (not written). B == 0, N == 0 or total_tokens == 0 is an
+ * empty problem: FATTN_OK, nothing launched.
+ * Errors: INVALID_ARG for null q/k/v/o, negative sizes, Hq % Hkv != 0,
+ *   non-finite scale, misaligned pointers; UNSUPPORTED for d not in {64, 128}.
+ */
+fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                       int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                       const int32_t* cu_seqlens, int total_tokens,
+                       fattn_dtype dtype, cudaStream_t stream);
+
+/*
+ * fattn_decode_workspace_size — bytes of scratch fattn_decode_paged needs:
+ * the per-split partials lse_part [B, Hq, S] fp32 and o_part [B, Hq, S, d]
+ * fp32 (S = num_splits), each region 256-byte aligned. Returns 0 for
+ * non-positive arguments.
+ */
+size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits);
+
+/*
+ * fattn_decode_paged — split-KV decode over a paged KV cache.
+ * [FA-LLM] "Decode is a different problem", "Flash-Decoding" (split the KV
+ * sequence across thread blocks, merge the partial (m, l, O) with the same
+ * online-softmax rule) and "Paged variants" (read K/V through a block table).
+ *
+ * q [B, Hq, d] bf16: one query token per sequence, which sees all seqlens[b]
+ *   keys of its sequence.
+ * kcache, vcache [num_pages, page_size, Hkv, d] bf16: the shared page pool.
+ * block_table DEVICE int32 [B, max_pages_per_seq]: logical page p of sequence
+ *   b is pool page block_table[b * max_pages_per_seq + p]. Entries past a
+ *   sequence's last page are never read.
+ * seqlens DEVICE int32 [B]: context length of each sequence, 0 <= seqlens[b]
+ *   <= max_pages_per_seq * page_size.
+ * num_splits = S >= 1: every sequence's pages are cut into S chunks of
+ *   C = ceil(max_pages_per_seq / S) whole pages; split s covers tokens
+ *   [s*C*page_size, min(seqlens[b], (s+1)*C*page_size)) and is empty past
+ *   the end of the sequence.
+ * o [B, Hq, d] bf16, lse [B, Hq] fp32 (lse may be NULL).
+ * workspace: device scratch of at least fattn_decode_workspace_size(B, Hq, d,
+ *   S) bytes, 256-byte aligned; after the call it holds the partials
+ *   (lse_part first, then o_part; each o_part row divided by its own l, and
+ *   lse_part = -inf for an empty split).
+ * Errors: INVALID_ARG (null/misaligned pointers, non-positive sizes,
+ *   Hq % Hkv != 0, non-finite scale), UNSUPPORTED (d not in {64, 128}),
+ *   WORKSPACE (workspace NULL or too small). A block-table entry outside
+ *   [0, num_pages) or a seqlens entry above the table's capacity is caught on
+ *   the device: the affected pages are skipped and FATTN_ERR_DEVICE_CHECK is
+ *   recorded in the status word.
+ */
+fattn_status fattn_decode_paged(const void* q, const void* kcache, const void* vcache,
+                                const int32_t* block_table, const int32_t* seqlens,
+                                int num_splits, void* o, float* lse,
+                                int B, int Hq, int Hkv, int d, int page_size,
+                                int max_pages_per_seq, int num_pages, float scale,
+                                void* workspace, size_t workspace_bytes,
+                                cudaStream_t stream);
+
+/*
+ * fattn_merge_partials — merge split partials with the online-softmax rule.
+ * [FA-LLM] "Flash-Decoding": each chunk's partial (m, l, O) is merged with
+ * the same rescaling rule.
+ *
+ * o_part [B, Hq, S, d] fp32 holds each split's output already divided by its
+ * own l; lse_part [B, Hq, S] fp32 its logsumexp (-inf = empty split, whose
+ * o_part row is never read). Output: lse = ln(sum_s e^{lse_s}),
+ * O = sum_s e^{lse_s - lse} O_s, written to o [B, Hq, d] in out_dtype and lse
+ * [B, Hq] fp32 (lse may be NULL). All splits empty gives O = 0, lse = -inf.
+ * Errors: INVALID_ARG (null/misaligned pointers, non-positive sizes),
+ * UNSUPPORTED (d not a positive multiple of 4 up to 512).
+ */
+fattn_status fattn_merge_partials(const float* o_part, const float* lse_part, void* o, float* lse,
+                                  int B, int Hq, int num_splits, int d, fattn_dtype out_dtype,
+                                  cudaStream_t stream);
+
+/* Static English description of a status code (never NULL). */
+const char* fattn_status_string(fattn_status status);
+
+/*
+ * fattn_debug_read_status — synchronise `stream`, then read and clear the
+ * device status word of the current device. Returns FATTN_OK if no device-side
+ * check failed since the last read, else the first recorded code
+ * (FATTN_ERR_TIMEOUT or FATTN_ERR_DEVICE_CHECK), or FATTN_ERR_CUDA if the
+ * synchronisation itself failed. Meant for tests and debugging: it blocks.
+ */
+fattn_status fattn_debug_read_status(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FATTN_H */

@@ -1,0 +1,43 @@
+"""Shared helpers for the GPU parity tests (no oracle arithmetic here)."""
+import numpy as np
+import pytest
+import torch
+
+# Tolerances against the fp64 oracle, on identical (bf16-rounded) inputs:
+# bf16 inputs with fp32 accumulation: O max abs <= 2e-2, O mean abs <= 2e-3,
+# lse max abs <= 1e-3; fp32 inputs: O max abs <= 1e-4 (lse held to the same).
+BF16_O_MAX = 2e-2
+BF16_O_MEAN = 2e-3
+LSE_MAX = 1e-3
+F32_O_MAX = 1e-4
+F32_LSE_MAX = 1e-4
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test run without a CUDA device")
+    from exact_tiled_attention_fattn_gb300 import build, fattn
+    build.build()
+    return fattn
+
+
+def as_np(t):
+    return t.detach().float().cpu().double().numpy()
+
+
+def check(o_gpu, lse_gpu, o_ref, lse_ref, fp32=False, what=""):
+    o = as_np(o_gpu) if isinstance(o_gpu, torch.Tensor) else o_gpu
+    err = np.abs(o - o_ref)
+    assert np.all(np.isfinite(o)), f"{what}: non-finite output"
+    if fp32:
+        assert err.max() <= F32_O_MAX, f"{what}: O max err {err.max():.3e}"
+    else:
+        assert err.max() <= BF16_O_MAX, f"{what}: O max err {err.max():.3e}"
+        assert err.mean() <= BF16_O_MEAN, f"{what}: O mean err {err.mean():.3e}"
+    if lse_gpu is not None:
+        lg = as_np(lse_gpu) if isinstance(lse_gpu, torch.Tensor) else lse_gpu
+        fin = np.isfinite(lse_ref)
+        assert np.array_equal(np.isfinite(lg), fin), f"{what}: lse finiteness differs"
+        lerr = np.abs(lg[fin] - lse_ref[fin]) if fin.any() else np.zeros(1)
+        assert lerr.max() <= (F32_LSE_MAX if fp32 else LSE_MAX), f"{what}: lse max err {lerr.max():.3e}"
+    return float(err.max()), float(err.mean())
