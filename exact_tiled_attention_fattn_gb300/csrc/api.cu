@@ -93,8 +93,10 @@ extern "C" const char* fattn_status_string(fattn_status s) {
 extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                                   int Hkv, int N, int d, int causal, float scale, const int32_t* cu_seqlens,
                                   int total_tokens, fattn_dtype dtype, cudaStream_t stream) {
-  if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || total_tokens < 0) return FATTN_ERR_INVALID_ARG;
+  // An empty problem is valid whatever the pointers (an empty tensor may have none).
+  if (B == 0 || N == 0 || (cu_seqlens && total_tokens == 0)) return FATTN_OK;
+  if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return FATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
   if (dtype != FATTN_BF16 && dtype != FATTN_FP32) return FATTN_ERR_INVALID_ARG;
@@ -103,7 +105,6 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
   if (cu_seqlens && (reinterpret_cast<uintptr_t>(cu_seqlens) & 3u)) return FATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
   const long long rows = cu_seqlens ? (long long)total_tokens : (long long)B * N;
-  if (B == 0 || N == 0 || rows == 0) return FATTN_OK;
   if (rows > 0x7fffffffLL || (long long)B * Hq * N > 0x7fffffffLL * 4LL) return FATTN_ERR_UNSUPPORTED;
 
   int err = 0;

@@ -116,6 +116,8 @@ def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None)
     v = _f64(v)
     nq, nk = q.shape[0], k.shape[0]
     rows = np.arange(nq) if rows is None else np.asarray(rows)
+    if nk == 0:                                        # no key at all: O = 0, lse = -inf
+        return np.zeros((len(rows), v.shape[-1])), np.full(len(rows), -np.inf)
     s = scale * (q[rows] @ k.T)
     ok = _allowed(rows, nk, nq, causal)
     s = np.where(ok, s, -np.inf)

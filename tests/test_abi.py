@@ -69,6 +69,7 @@ def test_fwd_validation(lib):
     assert _fwd(lib, B=0) == E.FATTN_OK
     assert _fwd(lib, N=0) == E.FATTN_OK
     assert _fwd(lib, cu=A, T=0, N=16) == E.FATTN_OK
+    assert _fwd(lib, B=0, q=None, k=None, v=None, o=None) == E.FATTN_OK   # empty tensors carry no pointer
 
 
 def _dec(lib, q=A, kc=A, vc=A, bt=A, sl=A, S=4, o=A, lse=A, B=2, Hq=8, Hkv=2, d=128, ps=16, maxp=8, pages=16,

@@ -225,6 +225,19 @@ def test_merge_of_split_partials_equals_unsplit(seed):
     assert np.max(np.abs(lse - lse_ref)) <= 1e-12
 
 
+def test_empty_key_set_is_zero_and_minus_inf():
+    """A row with no visible key (empty context) has O = 0 and lse = -inf; as a split it has no weight."""
+    o, lse = orc.attention_definition(np.ones((2, 4)), np.zeros((0, 4)), np.zeros((0, 3)), 1.0)
+    assert np.array_equal(o, np.zeros((2, 3))) and np.all(np.isneginf(lse))
+    rng = np.random.default_rng(14)
+    q, k, v = _rand(rng, 2, 4), _rand(rng, 6, 4), _rand(rng, 6, 3)
+    o_ref, l_ref = orc.attention_definition(q, k, v, 1.0)
+    lp = np.stack([lse, l_ref], axis=-1)
+    op = np.stack([o, o_ref], axis=1)
+    om, lm = orc.merge_partials(lp, op)
+    assert np.max(np.abs(om - o_ref)) <= 1e-15 and np.max(np.abs(lm - l_ref)) <= 1e-15
+
+
 def test_merge_all_empty_is_zero_and_minus_inf():
     o, lse = orc.merge_partials(np.full((2, 4), -np.inf), np.ones((2, 4, 3)))
     assert np.array_equal(o, np.zeros((2, 3)))
