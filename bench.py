@@ -44,6 +44,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
+    ap.add_argument("--profile-once", action="store_true",
+                    help="one prefill and one decode launch on the bench workloads, then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -72,7 +74,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -210,6 +212,16 @@ def main():
 
     def decode():
         fattn.decode_paged(dq, dk, dv, dbt, dsl, S, scale=dec.scale, out=do, lse=dlse, workspace=ws)
+
+    if args.profile_once:
+        prefill()
+        decode()
+        torch.cuda.synchronize()
+        st = fattn.debug_read_status()
+        print(json.dumps({"profile_once": True, "num_splits": S, "device_status": st}), flush=True)
+        if st != 0:
+            raise SystemExit(1)
+        return
 
     for _ in range(max(3, args.warmup)):
         flush.zero_()
