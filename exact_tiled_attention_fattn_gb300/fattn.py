@@ -34,6 +34,8 @@ SIGNATURES = {
     "fattn_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fattn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz,
                                 _vp]),
+    "fattn_decode_paged_static": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f,
+                                       _vp]),
     "fattn_merge_partials": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
     "fattn_debug_read_status": (_i, [_vp]),
@@ -181,6 +183,36 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, num_splits: int, scale
                                 _ptr(out), _ptr(lse), B, Hq, Hkv, d, page_size, maxp, num_pages, float(scale),
                                 _ptr(workspace), ws_bytes, ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_decode_paged", st)
+    return out, lse
+
+
+# Size of the fixed device scratch behind decode_paged_static (FATTN_DECODE_STATIC_SCRATCH_BYTES).
+DECODE_STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def decode_paged_static(q, kcache, vcache, block_table, seqlens, num_splits: int, scale: float | None = None,
+                        out=None, lse=None, want_lse: bool = True, stream=None):
+    """decode_paged for callers that cannot allocate a device workspace: the split
+    partials live in the library's fixed 32 MiB device scratch. Calls share that
+    scratch, so calls that overlap on the GPU race; the first call on a device
+    looks up the scratch address and should come before any stream capture."""
+    lib = load_library()
+    _need_cuda(q, kcache, vcache, block_table, seqlens, out, lse)
+    if block_table.dtype != torch.int32 or seqlens.dtype != torch.int32:
+        raise TypeError("block_table and seqlens must be int32")
+    B, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = kcache.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    st = lib.fattn_decode_paged_static(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table), _ptr(seqlens),
+                                       num_splits, _ptr(out), _ptr(lse), B, Hq, Hkv, d, page_size,
+                                       block_table.shape[1], num_pages, float(scale),
+                                       ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_decode_paged_static", st)
     return out, lse
 
 

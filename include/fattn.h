@@ -149,6 +149,38 @@ fattn_status fattn_merge_partials(const float* o_part, const float* lse_part, vo
                                   int B, int Hq, int num_splits, int d, fattn_dtype out_dtype,
                                   cudaStream_t stream);
 
+/*
+ * fattn_decode_paged_static — fattn_decode_paged without a workspace, for
+ * callers that cannot allocate device memory. The pages have no counterpart:
+ * this is library plumbing. Some callers cannot call cudaMalloc: plugins whose
+ * host (an inference server or another runtime) hands them only their input
+ * and output buffers, and code that must stay inside a device-memory budget
+ * owned by a pool it cannot draw from. This call runs the same kernels as
+ * fattn_decode_paged, with the split partials kept in a fixed scratch array
+ * of FATTN_DECODE_STATIC_SCRATCH_BYTES (32 MiB) that is part of the library's
+ * device image: every GPU that loads the library holds it until the process
+ * exits. The call allocates and frees nothing.
+ *
+ * Arguments, layouts and outputs are those of fattn_decode_paged minus the
+ * workspace. The first call on a device (with that device current) looks up
+ * the scratch's device address with cudaGetSymbolAddress and caches it; make
+ * that first call before any stream capture on that device. All calls share
+ * the one scratch array, which keeps the last call's contents (every partial
+ * a call reads back is written by that same call, so nothing needs clearing):
+ * calls that overlap on the GPU — on different streams, or from different
+ * host threads — race on it and must be serialised by the caller.
+ * Errors: those of fattn_decode_paged; FATTN_ERR_WORKSPACE when the partials
+ * (fattn_decode_workspace_size(B, Hq, d, num_splits) bytes) exceed the
+ * scratch; FATTN_ERR_CUDA if the scratch address cannot be obtained.
+ */
+#define FATTN_DECODE_STATIC_SCRATCH_BYTES ((size_t)32 << 20)
+fattn_status fattn_decode_paged_static(const void* q, const void* kcache, const void* vcache,
+                                       const int32_t* block_table, const int32_t* seqlens,
+                                       int num_splits, void* o, float* lse,
+                                       int B, int Hq, int Hkv, int d, int page_size,
+                                       int max_pages_per_seq, int num_pages, float scale,
+                                       cudaStream_t stream);
+
 /* Static English description of a status code (never NULL). */
 const char* fattn_status_string(fattn_status status);
 

@@ -33,7 +33,8 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == {"fattn_fwd", "fattn_decode_workspace_size", "fattn_decode_paged",
-                          "fattn_merge_partials", "fattn_status_string", "fattn_debug_read_status"}
+                          "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
+                          "fattn_debug_read_status"}
 
 
 def test_status_strings(lib):
