@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import concurrent.futures as cf
 import os
+import re
 import shutil
 import subprocess
 import sys
@@ -46,6 +47,27 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
+# The tensor-core prefill splits its launch registers between warpgroups with
+# setmaxnreg, assuming ptxas launches it at this many registers per thread; a
+# different count would make the split wait forever, so the build refuses it.
+PREFILL_TC_LAUNCH_REGS = 168
+
+
+def _check_launch_registers(ptxas_log: str):
+    counts = []
+    lines = ptxas_log.splitlines()
+    for i, line in enumerate(lines):
+        if "Compiling entry function" in line and "prefill_tc_kernel" in line:
+            for nxt in lines[i + 1:i + 4]:
+                m = re.search(r"Used (\d+) registers", nxt)
+                if m:
+                    counts.append(int(m.group(1)))
+                    break
+    if not counts or any(c != PREFILL_TC_LAUNCH_REGS for c in counts):
+        raise RuntimeError(f"prefill_tc_kernel launch registers {counts} != {PREFILL_TC_LAUNCH_REGS}: "
+                           "the setmaxnreg split in prefill_tc.cu must be recomputed")
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile and link libfattn.so unless it is newer than every source."""
     if not force and up_to_date():
@@ -55,14 +77,14 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *CFLAGS, *ARCH, "-c", src, "-o", obj]
-        if verbose:
-            cmd.insert(1, "-Xptxas=-v")
+        cmd = [nvcc, *CFLAGS, *ARCH, "-Xptxas=-v", "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
         if verbose and r.stderr:
             print(r.stderr, file=sys.stderr)
+        if os.path.basename(src) == "prefill_tc.cu":
+            _check_launch_registers(r.stderr)
         return obj
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:

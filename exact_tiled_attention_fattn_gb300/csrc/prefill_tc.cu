@@ -2,19 +2,33 @@
 // online-softmax rule ("The trick: tiles and an online softmax", FlashAttention
 // LLM-inference page; "The forward pass", FlashAttention explained).
 //
-// One CTA per SM loops over work items (sequence, query head, 128-row Q tile).
-// Roles (warp-specialised):
-//   warp 0      TMA producer: Q tile once per item, then K_j / V_j tiles into
-//               two 2-stage rings (128-byte swizzle, 64-column boxes).
-//   warp 1      MMA issuer (one thread): S_j = Q K_j^T into one of two TMEM
-//               score buffers, O += P_j V_j with P_j read from TMEM.
-//   warps 2-5   softmax: each thread owns one query row (TMEM lane). It loads
-//               its 128 scores, masks (causal diagonal, sequence end), keeps
-//               the running max m and sum l in registers, writes P_j (bf16) to
-//               TMEM, rescales O in TMEM by e^{m-m'} when the max moved, and
-//               at the end writes O / l (bf16) and lse = m + ln l.
+// One CTA per SM loops over work items (sequence, query head, 256 query rows =
+// two 128-row Q tiles A and B that share every K/V tile). Roles:
+//   warp 0      TMA producer: Q_A and Q_B once per item, then K_j / V_j tiles
+//               into two 2-stage rings (128-byte swizzle, 64-column boxes).
+//   warp 1      MMA issuer (one thread). Per K/V tile j it issues
+//               O_A += P_A(j-1) V_{j-1}, S_A = Q_A K_j^T, O_B += P_B(j-1) V_{j-1},
+//               S_B = Q_B K_j^T, so that while one softmax warpgroup works on its
+//               scores the tensor core runs the other tile's two products.
+//   warps 2-3   idle (they complete the first warpgroup, which gives registers
+//               to the softmax warpgroups with setmaxnreg).
+//   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread owns
+//               one query row (TMEM lane); it loads its 128 scores, masks (causal
+//               diagonal, sequence end), keeps the running max m and sum l in
+//               registers, writes P (bf16) over the first 64 columns of its S
+//               buffer, rescales O in TMEM when the max moved, and at the end
+//               writes O / l (bf16) and lse = m + ln l.
+// The running max is raised lazily: a row keeps its old m while no new score
+// exceeds it by more than 2^8 (p <= 256 then, exact in the final O/l because O
+// and l use the same m), which makes the O rescale rare.
 // Causal tiles above the diagonal are never loaded or computed ("tiles above
 // the diagonal are never touched"). S and P never leave the SM.
+//
+// P_X aliases S_X: S_X(j) is issued right after O_X += P_X(j-1) V by the same
+// thread, and tcgen05.mma operations issued by one thread execute in order, so
+// the product has read P_X(j-1) before S_X(j) overwrites those columns. The
+// softmax writes P_X(j) only after S_X(j) completed, whose commit covers every
+// earlier MMA, O_X += P_X(j-1) V included.
 //
 // Every pipeline wait is bounded: a wait that exceeds its limit records
 // FATTN_ERR_TIMEOUT in the device status word, every role stops, in-flight
@@ -31,58 +45,105 @@ namespace {
 using namespace sm100;
 
 constexpr int BM = 128;          // query rows per tile (M of one tcgen05.mma)
-constexpr int BN = 128;          // keys per tile
-constexpr int kThreads = 192;    // 6 warps
+constexpr int BN = 128;          // keys per K/V tile
+constexpr int kRowsPerItem = 2 * BM;
+constexpr int kThreads = 384;    // 3 warpgroups
+// Register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded
+// down to the allocation granularity), i.e. 384 * 168 = 64512 in total. The
+// producer/MMA warpgroup drops to 88 and the two softmax warpgroups rise to 208:
+// 128 * 88 + 256 * 208 = 64512. The build checks that ptxas launches this
+// kernel at exactly kRegsLaunch registers.
+constexpr int kRegsLaunch = 168;
+constexpr int kRegsControl = 88;
+constexpr int kRegsSoftmax = 208;
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
+constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exceed it by <= 2^8
 
 template <int D>
 struct TcLayout {
-  static constexpr int kQBytes = BM * D * 2;
+  static constexpr int kQBytes = BM * D * 2;      // one Q tile
   static constexpr int kKVBytes = BN * D * 2;
   static constexpr int kStages = 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffQ = 0;                 // Q_A then Q_B
+  static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-  static constexpr int kNumBars = 16;
+  static constexpr int kNumBars = 17;
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would block in tcgen05.alloc) never shares the SM
   static constexpr int kUsed = kOffAbort + 8 + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
-  // TMEM columns: two fp32 score buffers, the fp32 output, two bf16 P buffers.
-  static constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256;
-  static constexpr uint32_t kColP0 = 256 + D, kColP1 = 256 + D + BN / 2;
-  static_assert(kColP1 + BN / 2 <= kTmemCols, "TMEM budget");
+  // TMEM columns: fp32 scores S_A, S_B (P_X in bf16 over their first 64 columns), fp32 O_A, O_B.
+  __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
+  __host__ __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
+  static_assert(256 + 2 * D <= kTmemCols, "TMEM budget");
 };
 
 // barrier slots
 enum : int {
   kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8,
-  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 15
+  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16
 };
 
 struct Item {
-  int b, h, mt, row0, L, n;
+  int b, h, base, row0, L;
+  int n[2];   // K/V tiles tile A / tile B must visit (0: tile B has no row of the sequence)
   bool valid;
 };
 
-__device__ __forceinline__ Item decode_item(const PrefillParams& p, int it, int tiles) {
+// Work-item order. Heads (b, h) are taken in groups whose items fill about two
+// rounds of the grid; inside a group the items go heaviest causal Q pair first
+// (all heads of the group at one pair index, then the next), and the grid walks
+// the item list in alternating direction round by round ("snake"), so each CTA
+// pairs heavy items with light ones while the K/V of the few heads in flight
+// stay in L2.
+struct Schedule {
+  int pairs, heads, group, total;
+};
+
+__device__ __forceinline__ Schedule make_schedule(const PrefillParams& p) {
+  Schedule s;
+  s.pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
+  s.heads = p.B * p.Hq;
+  const int G = p.Hq / p.Hkv;
+  int grp = (2 * (int)gridDim.x + s.pairs - 1) / s.pairs;   // heads per group
+  grp = ((grp + G - 1) / G) * G;                            // whole GQA groups
+  s.group = grp < s.heads ? grp : s.heads;
+  s.total = s.heads * s.pairs;
+  return s;
+}
+
+// k-th item of this CTA, or -1 past the end.
+__device__ __forceinline__ int item_index(const Schedule& s, int k) {
+  const int G = (int)gridDim.x;
+  const int idx = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return idx < s.total ? idx : -1;
+}
+
+__device__ __forceinline__ Item decode_item(const PrefillParams& p, const Schedule& s, int it) {
   Item x;
-  const int bh = it / tiles;
-  x.mt = tiles - 1 - (it - bh * tiles);  // heaviest Q tile of a head first
+  const int per_group = s.group * s.pairs;
+  const int g = it / per_group;
+  const int rem = it - g * per_group;
+  const int gh = min(s.group, s.heads - g * s.group);       // heads in this (maybe last) group
+  const int rank = rem / gh;
+  const int bh = g * s.group + (rem - rank * gh);
+  const int pair = s.pairs - 1 - rank;
   x.b = bh / p.Hq;
   x.h = bh - x.b * p.Hq;
+  x.base = pair * kRowsPerItem;
   if (p.cu_seqlens) {
     const int start = __ldg(p.cu_seqlens + x.b);
     const int end = __ldg(p.cu_seqlens + x.b + 1);
     if (start < 0 || end < start || end > p.total_rows || end - start > p.N) {
       x.valid = false;
-      x.row0 = x.L = x.n = 0;
-      if (x.mt == 0 && x.h == 0 && (threadIdx.x & 31) == 0) record_status(p.status, kStatusDeviceCheck);
+      x.row0 = x.L = x.n[0] = x.n[1] = 0;
+      if (pair == 0 && x.h == 0 && (threadIdx.x & 31) == 0) record_status(p.status, kStatusDeviceCheck);
       return x;
     }
     x.row0 = start;
@@ -91,9 +152,16 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, int it, int 
     x.row0 = x.b * p.N;
     x.L = p.N;
   }
-  x.valid = x.mt * BM < x.L;
+  x.valid = x.base < x.L;
   const int kv_tiles = (x.L + BN - 1) / BN;
-  x.n = p.causal ? min(x.mt + 1, kv_tiles) : kv_tiles;
+  const bool has_b = x.base + BM < x.L;
+  if (p.causal) {
+    x.n[0] = min(x.base / BN + 1, kv_tiles);
+    x.n[1] = has_b ? min((x.base + BM) / BN + 1, kv_tiles) : 0;
+  } else {
+    x.n[0] = kv_tiles;
+    x.n[1] = has_b ? kv_tiles : 0;
+  }
   return x;
 }
 
@@ -114,6 +182,36 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok;
 }
 
+// ---- packed fp32 pairs (sm_100 f32x2 arithmetic) ----
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -127,7 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < Lay::kNumBars; ++i) mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
+    for (int i = 0; i < Lay::kNumBars; ++i)
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -145,24 +244,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kOffHolder);
 
-  const int tiles = (p.N + BM - 1) / BM;
-  const int num_items = p.B * p.Hq * tiles;
+  const Schedule sch = make_schedule(p);
   const int G = p.Hq / p.Hkv;
 
+  if (warp < 4) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       uint32_t nq = 0, nk = 0, nv = 0;
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
-      for (int it = blockIdx.x; it < num_items; it += gridDim.x) {
-        const Item x = decode_item(p, it, tiles);
+      for (int k = 0;; ++k) {
+        const int it = item_index(sch, k);
+        if (it < 0) break;
+        const Item x = decode_item(p, sch, it);
         if (!x.valid) continue;
         const int hkv = x.h / G;
+        const int n = max(x.n[0], x.n[1]);
         if (!mbar_wait(bar(kBarQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(bar(kBarQFull), Lay::kQBytes);
+        mbar_arrive_expect_tx(bar(kBarQFull), 2 * Lay::kQBytes);
 #pragma unroll
-        for (int dc = 0; dc < D / 64; ++dc)
-          tma_load_3d(sb + Lay::kOffQ + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h, x.row0 + x.mt * BM, pol_q);
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int dc = 0; dc < D / 64; ++dc)
+            tma_load_3d(sb + Lay::kOffQ + t * Lay::kQBytes + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h,
+                        x.row0 + x.base + t * BM, pol_q);
         ++nq;
         auto load_k = [&](int j) -> bool {
           const uint32_t st = nk & 1;
@@ -186,10 +292,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nv;
           return true;
         };
-        // same order the MMA warp consumes them: K0 K1 V0 K2 V1 K3 V2 ...
-        bool ok = load_k(0) && (x.n < 2 || load_k(1)) && load_v(0);
-        for (int j = 2; ok && j < x.n; ++j) ok = load_k(j) && load_v(j - 1);
-        if (ok && x.n > 1) ok = load_v(x.n - 1);
+        // the order the MMA warp consumes them: K0 K1 V0 K2 V1 K3 V2 ...
+        bool ok = load_k(0) && (n < 2 || load_k(1)) && load_v(0);
+        for (int j = 2; ok && j < n; ++j) ok = load_k(j) && load_v(j - 1);
+        if (ok && n > 1) ok = load_v(n - 1);
         if (!ok) break;
       }
       // no copy may land after the CTA is gone: wait for the last armed phase of each barrier
@@ -205,92 +311,129 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);  // Q K^T: both K-major
       constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);   // P V: V is MN-major (d contiguous)
-      uint32_t nq = 0, nk = 0, nv = 0, gs = 0;
+      uint32_t nq = 0, nk = 0, nv = 0;
+      uint32_t np[2] = {0, 0};                             // P_X buffers consumed so far
+      auto issue_s = [&](int t, uint32_t kst) {
+        const uint32_t d_tmem = tmem + Lay::col_s(t);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t a = sb + Lay::kOffQ + t * Lay::kQBytes + (ks >> 2) * BM * 128 + (ks & 3) * 32;
+          const uint32_t b = sb + Lay::kOffK + kst * Lay::kKVBytes + (ks >> 2) * BN * 128 + (ks & 3) * 32;
+          mma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(kBarSFull + t));
+      };
+      auto issue_pv = [&](int t, uint32_t vst, bool acc) -> bool {
+        if (!mbar_wait(bar(kBarPFull + t), np[t] & 1, abort, p.status, kWaitLimitNs)) return false;
+        ++np[t];
+        tc_fence_after();
+        const uint32_t p_tmem = tmem + Lay::col_s(t);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks) {
+          const uint32_t b = sb + Lay::kOffV + vst * Lay::kKVBytes + ks * 16 * 128;
+          mma_ts(tmem + Lay::col_o(t), p_tmem + ks * 8, smem_desc_sw128(b, BN * 128, 1024), idO,
+                 (acc || ks > 0) ? 1u : 0u);
+        }
+        return true;
+      };
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < num_items; it += gridDim.x) {
-        const Item x = decode_item(p, it, tiles);
+      for (int k = 0; ok; ++k) {
+        const int it = item_index(sch, k);
+        if (it < 0) break;
+        const Item x = decode_item(p, sch, it);
         if (!x.valid) continue;
+        const int nA = x.n[0], nB = x.n[1];
+        const int n = max(nA, nB);
         if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
         ++nq;
         tc_fence_after();
-        auto issue_s = [&](uint32_t g) -> bool {
-          const uint32_t st = nk & 1;
-          if (!mbar_wait(bar(kBarKFull + st), (nk >> 1) & 1, abort, p.status, kWaitLimitNs)) return false;
+        // j = 0
+        {
+          const uint32_t kst = nk & 1;
+          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
           tc_fence_after();
-          const uint32_t d_tmem = tmem + ((g & 1) ? Lay::kColS1 : Lay::kColS0);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t a = sb + Lay::kOffQ + (ks >> 2) * BM * 128 + (ks & 3) * 32;
-            const uint32_t b = sb + Lay::kOffK + st * Lay::kKVBytes + (ks >> 2) * BN * 128 + (ks & 3) * 32;
-            mma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idS, ks > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(kBarKEmpty + st));
-          mma_commit(bar(kBarSFull + (g & 1)));
+          issue_s(0, kst);
+          if (nB > 0) issue_s(1, kst);
+          mma_commit(bar(kBarKEmpty + kst));
           ++nk;
-          return true;
-        };
-        ok = issue_s(gs) && (x.n < 2 || issue_s(gs + 1));
-        if (ok && x.n <= 2) mma_commit(bar(kBarQEmpty));
-        for (int j = 0; ok && j < x.n; ++j) {
-          const uint32_t g = gs + j;
-          if (!mbar_wait(bar(kBarPFull + (g & 1)), (g >> 1) & 1, abort, p.status, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t st = nv & 1;
-          if (!mbar_wait(bar(kBarVFull + st), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t p_tmem = tmem + ((g & 1) ? Lay::kColP1 : Lay::kColP0);
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks) {
-            const uint32_t b = sb + Lay::kOffV + st * Lay::kKVBytes + ks * 16 * 128;
-            mma_ts(tmem + Lay::kColO, p_tmem + ks * 8, smem_desc_sw128(b, BN * 128, 1024), idO,
-                   (j > 0 || ks > 0) ? 1u : 0u);
-          }
-          mma_commit(bar(kBarVEmpty + st));
-          mma_commit(bar(kBarOFull));
-          ++nv;
-          if (j + 2 < x.n) {
-            if (!issue_s(g + 2)) {
-              ok = false;
-              break;
-            }
-            if (j + 2 == x.n - 1) mma_commit(bar(kBarQEmpty));
-          }
+          if (n == 1) mma_commit(bar(kBarQEmpty));
         }
-        gs += x.n;
+        for (int j = 1; ok && j < n; ++j) {
+          const uint32_t kst = nk & 1, vst = nv & 1;
+          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
+              !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (j - 1 < nA) {
+            if (!issue_pv(0, vst, j - 1 > 0)) { ok = false; break; }
+            if (j - 1 == nA - 1) mma_commit(bar(kBarOFull + 0));
+          }
+          if (j < nA) issue_s(0, kst);
+          if (j - 1 < nB) {
+            if (!issue_pv(1, vst, j - 1 > 0)) { ok = false; break; }
+            if (j - 1 == nB - 1) mma_commit(bar(kBarOFull + 1));
+          }
+          if (j < nB) issue_s(1, kst);
+          mma_commit(bar(kBarKEmpty + kst));
+          mma_commit(bar(kBarVEmpty + vst));
+          ++nk;
+          ++nv;
+          if (j == n - 1) mma_commit(bar(kBarQEmpty));
+        }
+        if (!ok) break;
+        // tail: the last P V of each tile
+        {
+          const uint32_t vst = nv & 1;
+          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
+          tc_fence_after();
+          if (n - 1 < nA) {
+            if (!issue_pv(0, vst, n - 1 > 0)) break;
+            mma_commit(bar(kBarOFull + 0));
+          }
+          if (n - 1 < nB) {
+            if (!issue_pv(1, vst, n - 1 > 0)) break;
+            mma_commit(bar(kBarOFull + 1));
+          }
+          mma_commit(bar(kBarVEmpty + vst));
+          ++nv;
+        }
       }
       // every MMA (and every commit before this one) has landed before TMEM is freed
       mma_commit(bar(kBarMmaDone));
       mbar_drain(bar(kBarMmaDone), 0);
     }
+  }
   } else {
-    // ------------------------------------------------------------ softmax
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    // ------------------------------------------------------------ softmax (tile t)
+    const int t = (warp - 4) >> 2;           // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may touch
     const int r = q4 * 32 + lane;            // query row within the tile
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + Lay::col_s(t);
+    const uint32_t o_col = tmem + lane_off + Lay::col_o(t);
     const float sl2 = p.scale * kLog2e;      // scores go to the log2 domain
     const bool neg = sl2 < 0.f;
-    uint32_t gs = 0;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    uint32_t ns = 0, no = 0;                 // S_t and O_t completions seen
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < num_items; it += gridDim.x) {
-      const Item x = decode_item(p, it, tiles);
-      if (!x.valid) continue;
-      const int row = x.mt * BM + r;
+    for (int k = 0; ok; ++k) {
+      const int it = item_index(sch, k);
+      if (it < 0) break;
+      const Item x = decode_item(p, sch, it);
+      if (!x.valid || x.n[t] == 0) continue;
+      const int row = x.base + t * BM + r;
       const int lim = p.causal ? min(row + 1, x.L) : x.L;  // keys < lim are visible
       float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; j < x.n; ++j) {
-        const uint32_t g = gs + j;
-        if (!warp_wait(bar(kBarSFull + (g & 1)), (g >> 1) & 1, abort, p.status)) {
+      for (int j = 0; j < x.n[t]; ++j) {
+        if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status)) {
           ok = false;
           break;
         }
+        ++ns;
         tc_fence_after();
-        const uint32_t s_col = tmem + lane_off + ((g & 1) ? Lay::kColS1 : Lay::kColS0);
         float s[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) {
@@ -306,85 +449,92 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < BN; ++c)
             if (kbase + c >= lim) s[c] = neg ? CUDART_INF_F : -CUDART_INF_F;
         }
-        float mx = s[0];
-        if (!neg) {
+        // row max (min for a negative scale): 8 independent chains of 3-input max
+        float mx;
+        {
+          float a[8];
 #pragma unroll
-          for (int c = 1; c < BN; ++c) mx = fmaxf(mx, s[c]);
-        } else {
+          for (int i = 0; i < 8; ++i) a[i] = s[i];
+          if (!neg) {
 #pragma unroll
-          for (int c = 1; c < BN; ++c) mx = fminf(mx, s[c]);
+            for (int c = 8; c < BN; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) a[i] = fmax3(a[i], s[c + i], s[c + 8 + i < BN ? c + 8 + i : c + i]);
+            mx = fmax3(fmax3(a[0], a[1], a[2]), fmax3(a[3], a[4], a[5]), fmaxf(a[6], a[7]));
+          } else {
+#pragma unroll
+            for (int c = 8; c < BN; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) a[i] = fmin3(a[i], s[c + i], s[c + 8 + i < BN ? c + 8 + i : c + i]);
+            mx = fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fminf(a[6], a[7]));
+          }
         }
-        const float m_new = fmaxf(m, mx * sl2);
+        const float m_cand = fmaxf(m, mx * sl2);
+        const bool need = m_cand > m + kLazyRescaleLog2;          // always true on the first tile
+        const float m_new = __any_sync(0xffffffffu, need) ? m_cand : m;
         const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
-        const float alpha = ex2(m - base);  // e^{m - m'}
-        float sum = 0.f;
+        const float alpha = ex2(m - base);                        // 1 when m is kept
+        const uint64_t nbase2 = f2_pack(-base, -base);
+        uint64_t acc2[4] = {0, 0, 0, 0};                          // +0.0f pairs
         uint32_t pk[BN / 2];
-        if (!masked) {
 #pragma unroll
-          for (int c = 0; c < BN; c += 2) {
-            const float p0 = ex2(fmaf(s[c], sl2, -base));
-            const float p1 = ex2(fmaf(s[c + 1], sl2, -base));
-            sum += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < BN; c += 2) {
+          float a0, a1;
+          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
+          float p0 = ex2(a0), p1 = ex2(a1);
+          if (masked) {
+            p0 = kbase + c < lim ? p0 : 0.f;
+            p1 = kbase + c + 1 < lim ? p1 : 0.f;
           }
-        } else {
-          const int vis = lim - kbase;  // keys [0, vis) of this tile are visible
-#pragma unroll
-          for (int c = 0; c < BN; c += 2) {
-            const float p0 = c < vis ? ex2(fmaf(s[c], sl2, -base)) : 0.f;
-            const float p1 = c + 1 < vis ? ex2(fmaf(s[c + 1], sl2, -base)) : 0.f;
-            sum += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
-          }
+          acc2[(c >> 1) & 3] = f2_add(acc2[(c >> 1) & 3], f2_pack(p0, p1));
+          pk[c / 2] = pack_bf16x2(p0, p1);
+        }
+        float sum;
+        {
+          float x0, x1;
+          f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), x0, x1);
+          sum = x0 + x1;
         }
         l = l * alpha + sum;
-        m = m_new;
-        if (j > 0) {
-          // PV_{g-1} has landed: O may be rescaled, and P buffer g&1 (read by PV_{g-2}) is free.
-          if (!warp_wait(bar(kBarOFull), (g - 1) & 1, abort, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          // O_t += P_t(j-1) V has completed (covered by the commit of S_t(j)).
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t u[32];
-              tmem_ld32(tmem + lane_off + Lay::kColO + 32 * c, u);
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(o_col + 32 * c, u);
 #pragma unroll
-              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-              tmem_st32(tmem + lane_off + Lay::kColO + 32 * c, u);
-            }
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st32(o_col + 32 * c, u);
           }
         }
-        const uint32_t p_col = tmem + lane_off + ((g & 1) ? Lay::kColP1 : Lay::kColP0);
+        m = m_new;
 #pragma unroll
         for (int c = 0; c < BN / 64; ++c) {
           uint32_t u[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = pk[32 * c + e];
-          tmem_st32(p_col + 32 * c, u);
+          tmem_st32(s_col + 32 * c, u);
         }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBarPFull + (g & 1)));
+        if (lane == 0) mbar_arrive(bar(kBarPFull + t));
       }
       if (!ok) break;
       // epilogue: O / l in bf16 and the row's logsumexp
-      if (!warp_wait(bar(kBarOFull), (gs + x.n - 1) & 1, abort, p.status)) {
+      if (!warp_wait(bar(kBarOFull + t), no & 1, abort, p.status)) {
         ok = false;
         break;
       }
+      ++no;
       tc_fence_after();
       const bool live = row < x.L;
       const float inv = 1.f / l;
-      __nv_bfloat16* orow =
-          static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
+      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem + lane_off + Lay::kColO + 32 * c, u);
+        tmem_ld32(o_col + 32 * c, u);
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -402,7 +552,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           p.lse[((size_t)x.b * p.Hq + x.h) * p.N + row] = lse;
       }
-      gs += x.n;
     }
   }
 
@@ -421,8 +570,8 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
-  const long long tiles = (p.N + BM - 1) / BM;
-  const long long items = (long long)p.B * p.Hq * tiles;
+  const long long pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
+  const long long items = (long long)p.B * p.Hq * pairs;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(items < num_sms ? items : num_sms);
   kern<<<grid, kThreads, Lay::kBytes, stream>>>(tq, tk, tv, p);
