@@ -196,11 +196,6 @@ __device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
-  uint64_t d;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-  return d;
-}
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -435,12 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ns;
         tc_fence_after();
         float s[BN];
+        {
+          uint32_t u[BN];
+          tmem_ld128(s_col, u);
 #pragma unroll
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t u[32];
-          tmem_ld32(s_col + 32 * c, u);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) s[32 * c + e] = __uint_as_float(u[e]);
+          for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(u[e]);
         }
         const int kbase = j * BN;
         const bool masked = kbase + BN > lim;  // causal diagonal tile or sequence end
@@ -475,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
         const float alpha = ex2(m - base);                        // 1 when m is kept
         const uint64_t nbase2 = f2_pack(-base, -base);
-        uint64_t acc2[4] = {0, 0, 0, 0};                          // +0.0f pairs
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 2) {
@@ -486,15 +480,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             p0 = kbase + c < lim ? p0 : 0.f;
             p1 = kbase + c + 1 < lim ? p1 : 0.f;
           }
-          acc2[(c >> 1) & 3] = f2_add(acc2[(c >> 1) & 3], f2_pack(p0, p1));
+          acc[(c >> 1) & 7] += p0 + p1;
           pk[c / 2] = pack_bf16x2(p0, p1);
         }
-        float sum;
-        {
-          float x0, x1;
-          f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), x0, x1);
-          sum = x0 + x1;
-        }
+        const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O_t += P_t(j-1) V has completed (covered by the commit of S_t(j)).
@@ -508,13 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         m = m_new;
-#pragma unroll
-        for (int c = 0; c < BN / 64; ++c) {
-          uint32_t u[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = pk[32 * c + e];
-          tmem_st32(s_col + 32 * c, u);
-        }
+        tmem_st64(s_col, pk);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
