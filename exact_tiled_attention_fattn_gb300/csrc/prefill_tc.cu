@@ -308,13 +308,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);   // P V: V is MN-major (d contiguous)
       uint32_t nq = 0, nk = 0, nv = 0;
       uint32_t np[2] = {0, 0};                             // P_X buffers consumed so far
+      // Descriptor bases, built once. The start-address field (bits 0-13, in
+      // 16-byte units) of each per-MMA descriptor is the base plus a
+      // compile-time offset, so issuing an MMA costs no descriptor arithmetic.
+      const uint64_t qd0 = smem_desc_sw128(sb + Lay::kOffQ, 16, 1024);
+      const uint64_t qd1 = smem_desc_sw128(sb + Lay::kOffQ + Lay::kQBytes, 16, 1024);
+      const uint64_t kd0 = smem_desc_sw128(sb + Lay::kOffK, 16, 1024);
+      const uint64_t kd1 = smem_desc_sw128(sb + Lay::kOffK + Lay::kKVBytes, 16, 1024);
+      const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, BN * 128, 1024);
+      const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, BN * 128, 1024);
       auto issue_s = [&](int t, uint32_t kst) {
         const uint32_t d_tmem = tmem + Lay::col_s(t);
+        const uint64_t a0 = t ? qd1 : qd0, b0 = kst ? kd1 : kd0;
+        mma_ss_c<false>(d_tmem, a0, b0, idS);
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t a = sb + Lay::kOffQ + t * Lay::kQBytes + (ks >> 2) * BM * 128 + (ks & 3) * 32;
-          const uint32_t b = sb + Lay::kOffK + kst * Lay::kKVBytes + (ks >> 2) * BN * 128 + (ks & 3) * 32;
-          mma_ss(d_tmem, smem_desc_sw128(a, 16, 1024), smem_desc_sw128(b, 16, 1024), idS, ks > 0 ? 1u : 0u);
+        for (int ks = 1; ks < D / 16; ++ks) {
+          constexpr int kAtomQ = BM * 128 / 16, kAtomK = BN * 128 / 16;  // 16-byte units per swizzle atom column
+          mma_ss_c<true>(d_tmem, a0 + (uint64_t)((ks >> 2) * kAtomQ + (ks & 3) * 2),
+                         b0 + (uint64_t)((ks >> 2) * kAtomK + (ks & 3) * 2), idS);
         }
         mma_commit(bar(kBarSFull + t));
       };
@@ -322,13 +333,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarPFull + t), np[t] & 1, abort, p.status, kWaitLimitNs)) return false;
         ++np[t];
         tc_fence_after();
-        const uint32_t p_tmem = tmem + Lay::col_s(t);
+        const uint32_t p_tmem = tmem + Lay::col_s(t), o_tmem = tmem + Lay::col_o(t);
+        const uint64_t b0 = vst ? vd1 : vd0;
+        mma_ts(o_tmem, p_tmem, b0, idO, acc ? 1u : 0u);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint32_t b = sb + Lay::kOffV + vst * Lay::kKVBytes + ks * 16 * 128;
-          mma_ts(tmem + Lay::col_o(t), p_tmem + ks * 8, smem_desc_sw128(b, BN * 128, 1024), idO,
-                 (acc || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 1; ks < BN / 16; ++ks) mma_ts_acc(o_tmem, p_tmem + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), idO);
         return true;
       };
       bool ok = true;
@@ -471,17 +480,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t nbase2 = f2_pack(-base, -base);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[BN / 2];
+        if (!masked) {
 #pragma unroll
-        for (int c = 0; c < BN; c += 2) {
-          float a0, a1;
-          f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
-          float p0 = ex2(a0), p1 = ex2(a1);
-          if (masked) {
-            p0 = kbase + c < lim ? p0 : 0.f;
-            p1 = kbase + c + 1 < lim ? p1 : 0.f;
+          for (int c = 0; c < BN; c += 2) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
+            const float p0 = ex2(a0), p1 = ex2(a1);
+            acc[(c >> 1) & 7] += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
           }
-          acc[(c >> 1) & 7] += p0 + p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        } else {
+          const int vis = lim - kbase;
+#pragma unroll
+          for (int c = 0; c < BN; c += 2) {
+            float a0, a1;
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
+            const float p0 = c < vis ? ex2(a0) : 0.f, p1 = c + 1 < vis ? ex2(a1) : 0.f;
+            acc[(c >> 1) & 7] += p0 + p1;
+            pk[c / 2] = pack_bf16x2(p0, p1);
+          }
         }
         const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * alpha + sum;
