@@ -64,7 +64,7 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int H, int d,
   return r == CUDA_SUCCESS;
 }
 
-int num_sms_current() {
+int num_sms_current() {  // declared in fattn_internal.h
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
@@ -135,7 +135,8 @@ static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 extern "C" size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
   size_t rows = (size_t)B * Hq * num_splits;
-  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float));
+  return align256(rows * sizeof(float)) + align256(rows * d * sizeof(float)) +
+         align256((size_t)(1 + B * Hq) * sizeof(int));
 }
 
 extern "C" fattn_status fattn_decode_paged(const void* q, const void* kcache, const void* vcache,
@@ -167,16 +168,15 @@ extern "C" fattn_status fattn_decode_paged(const void* q, const void* kcache, co
   const size_t rows = (size_t)B * Hq * num_splits;
   p.lse_part = static_cast<float*>(workspace);
   p.o_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)));
+  p.counters = reinterpret_cast<int*>(static_cast<char*>(workspace) + align256(rows * sizeof(float)) +
+                                      align256(rows * d * sizeof(float)));
+  p.o = o;
+  p.lse = lse;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.d = d; p.page_size = page_size; p.max_pages_per_seq = max_pages_per_seq;
   p.num_pages = num_pages; p.num_splits = num_splits; p.scale = scale;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
-  if (launch_decode_partials(p, stream) != cudaSuccess) return FATTN_ERR_CUDA;
-
-  MergeParams m;
-  m.o_part = p.o_part; m.lse_part = p.lse_part; m.o = o; m.lse = lse;
-  m.B = B; m.Hq = Hq; m.S = num_splits; m.d = d; m.out_bf16 = 1;
-  return launch_merge(m, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_decode(p, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" fattn_status fattn_merge_partials(const float* o_part, const float* lse_part, void* o, float* lse, int B,

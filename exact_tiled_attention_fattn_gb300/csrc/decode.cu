@@ -3,15 +3,19 @@
 // online-softmax rule.
 //
 // Decode is bound by HBM bandwidth: one query row per (sequence, head) meets a
-// long K/V. One CTA handles one (sequence, KV head, split) and all query heads
-// of that KV head's GQA group (up to 16 per CTA), so each K/V byte is read
-// once. Each of the 4 warps streams its own 16-token chunks through a 3-stage
+// long K/V. A persistent grid takes work items (sequence, KV head, split) from
+// a counter in the workspace, highest split first; an item covers all query
+// heads of that KV head's GQA group (up to 16), so each K/V byte is read once,
+// and an empty split costs one atomic instead of a thread block. Each of the 4 warps streams its own 16-token chunks through a 3-stage
 // cp.async pipeline (16-byte copies, L1 bypassed), finds each token's page
 // through the block table, and runs the two small products on the tensor
 // cores with mma.sync (S = Q K^T with the group's heads as the 16 rows,
 // O += P V with P kept in registers). Each warp keeps its own running (m, l, O)
 // and the four states are merged in shared memory with the same rescaling
-// rule at the end.
+// rule at the end. The CTA that finishes the last non-empty split of a
+// (sequence, KV-head group) merges that group's partials into the output
+// ("Flash-Decoding": partials merged with the same online-softmax rule), so no
+// separate merge launch is needed.
 #include "device_common.cuh"
 #include "fattn_internal.h"
 
@@ -73,40 +77,17 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Partial (lse_s, O_s / l_s) of one non-empty split [t0, t1) of sequence b
+// for the query heads h0 .. h0 + rows_valid - 1 of KV head hkv.
 template <int D, bool kPage16>
-__global__ void __launch_bounds__(kWarps * 32) decode_partials_kernel(const DecodeParams p) {
+__device__ __forceinline__ void decode_split(const DecodeParams& p, uint8_t* smem, int split, int b, int hkv, int h0,
+                                             int rows_valid, int t0, int t1) {
   using Lay = DecodeLayout<D>;
   constexpr int U = D / 8;
-  extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   const uint32_t q_base = sbase + Lay::kKvUnits * 16;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int split = blockIdx.x;
-  const int G = p.Hq / p.Hkv;
-  const int nsub = (G + 15) >> 4;
-  const int hkv = blockIdx.y / nsub, sub = blockIdx.y - hkv * nsub;
-  const int b = blockIdx.z;
-  const int rows_valid = min(16, G - sub * 16);
-  const int h0 = hkv * G + sub * 16;
-
-  // ---- token range of this split (whole pages, common chunk length) ----
-  const int cap = p.max_pages_per_seq * p.page_size;
-  int L = p.seqlens[b];
-  if (L < 0 || L > cap) {
-    if (threadIdx.x == 0) record_status(p.status, kStatusDeviceCheck);
-    L = L < 0 ? 0 : cap;
-  }
-  const int chunk_pages = (p.max_pages_per_seq + p.num_splits - 1) / p.num_splits;
-  const long long span = (long long)chunk_pages * p.page_size;
-  const long long t0ll = (long long)split * span;
   const size_t prow0 = ((size_t)b * p.Hq + h0) * p.num_splits + split;  // partial row of head h0
-  if (t0ll >= L) {
-    if (threadIdx.x < rows_valid) p.lse_part[prow0 + (size_t)threadIdx.x * p.num_splits] = -CUDART_INF_F;
-    return;
-  }
-  const int t0 = (int)t0ll;
-  const int t1 = (int)min((long long)L, t0ll + span);
   const int nchunks = (t1 - t0 + kChunk - 1) / kChunk;
 
   // ---- Q rows of the group (rows past the group are zero) ----
@@ -310,6 +291,92 @@ __global__ void __launch_bounds__(kWarps * 32) decode_partials_kernel(const Deco
   }
 }
 
+// Output rows of one (sequence, KV-head group) from its nvalid non-empty
+// split partials: lse = ln sum_s e^{lse_s}, O = sum_s e^{lse_s - lse} O_s.
+template <int D>
+__device__ __forceinline__ void merge_group(const DecodeParams& p, int b, int h0, int rows_valid, int nvalid) {
+  constexpr int C4 = D / 4;
+  for (int idx = threadIdx.x; idx < rows_valid * C4; idx += kWarps * 32) {
+    const int r = idx / C4, c = (idx - r * C4) * 4;
+    const size_t prow = ((size_t)b * p.Hq + h0 + r) * p.num_splits;
+    float m = -CUDART_INF_F;
+    for (int sp = 0; sp < nvalid; ++sp) m = fmaxf(m, __ldcg(p.lse_part + prow + sp));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    if (m != -CUDART_INF_F) {
+#pragma unroll 4
+      for (int sp = 0; sp < nvalid; ++sp) {
+        const float ls = __ldcg(p.lse_part + prow + sp);
+        const float w = ls == -CUDART_INF_F ? 0.f : ex2((ls - m) * kLog2e);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.o_part + (prow + sp) * D + c));
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+        wsum += w;
+      }
+    }
+    const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+    pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.o) + ((size_t)b * p.Hq + h0 + r) * D + c) = pk;
+    if (p.lse && c == 0) p.lse[(size_t)b * p.Hq + h0 + r] = wsum > 0.f ? m + logf(wsum) : -CUDART_INF_F;
+  }
+}
+
+template <int D, bool kPage16>
+__global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int s_item, s_last;
+  const int G = p.Hq / p.Hkv;
+  const int nsub = (G + 15) >> 4;
+  const int groups_per_seq = p.Hkv * nsub;
+  const int groups = p.B * groups_per_seq;
+  const int total = p.num_splits * groups;
+  const int cap = p.max_pages_per_seq * p.page_size;
+  const int chunk_pages = (p.max_pages_per_seq + p.num_splits - 1) / p.num_splits;
+  const long long span = (long long)chunk_pages * p.page_size;
+  for (;;) {
+    if (threadIdx.x == 0) s_item = atomicAdd(p.counters, 1);
+    __syncthreads();
+    const int item = s_item;
+    __syncthreads();
+    if (item >= total) break;
+    // highest split first: the long sequences' far chunks start early, empty items go fast
+    const int split = p.num_splits - 1 - item / groups;
+    const int g = item - (item / groups) * groups;
+    const int b = g / groups_per_seq;
+    const int hg = g - b * groups_per_seq;
+    const int hkv = hg / nsub, sub = hg - hkv * nsub;
+    const int rows_valid = min(16, G - sub * 16);
+    const int h0 = hkv * G + sub * 16;
+    int L = __ldg(p.seqlens + b);
+    if (L < 0 || L > cap) {
+      if (threadIdx.x == 0 && split == 0) record_status(p.status, kStatusDeviceCheck);
+      L = L < 0 ? 0 : cap;
+    }
+    const int nvalid = (int)((L + span - 1) / span);   // non-empty splits of this sequence
+    const long long t0 = (long long)split * span;
+    if (t0 >= L) {  // empty split: mark it, and a sequence with no key at all gets O = 0, lse = -inf
+      if (threadIdx.x < rows_valid)
+        p.lse_part[((size_t)b * p.Hq + h0 + threadIdx.x) * p.num_splits + split] = -CUDART_INF_F;
+      if (split == 0) merge_group<D>(p, b, h0, rows_valid, 0);
+      continue;
+    }
+    decode_split<D, kPage16>(p, smem, split, b, hkv, h0, rows_valid, (int)t0, (int)min((long long)L, t0 + span));
+    // publish the partial, count it, and let the last split of the group merge
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(p.counters + 1 + g, 1) == nvalid - 1;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      merge_group<D>(p, b, h0, rows_valid, nvalid);
+    }
+  }
+}
+
 // One CTA per (sequence, head) row: the splits are shared among groups of
 // threads, each thread owning 4 consecutive output elements.
 __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
@@ -387,18 +454,28 @@ __global__ void __launch_bounds__(128) merge_kernel(const MergeParams p) {
 template <int D, bool kPage16>
 cudaError_t launch_decode_t(const DecodeParams& p, cudaStream_t stream) {
   using Lay = DecodeLayout<D>;
-  auto kern = decode_partials_kernel<D, kPage16>;
+  auto kern = decode_kernel<D, kPage16>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Lay::kBytes);
   if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kWarps * 32, Lay::kBytes);
+  if (e != cudaSuccess) return e;
+  const int sms = num_sms_current();
+  if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidValue;
+  // work counter + one arrival counter per (sequence, KV-head group) start at zero
+  e = cudaMemsetAsync(p.counters, 0, (size_t)(1 + p.B * p.Hq) * sizeof(int), stream);
+  if (e != cudaSuccess) return e;
   const int G = p.Hq / p.Hkv;
-  dim3 grid(p.num_splits, p.Hkv * ((G + 15) / 16), p.B);
+  const long long items = (long long)p.num_splits * p.B * p.Hkv * ((G + 15) / 16);
+  const long long slots = (long long)sms * per_sm;
+  const int grid = (int)(items < slots ? items : slots);
   kern<<<grid, kWarps * 32, Lay::kBytes, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream) {
   const bool p16 = p.page_size == 16;
   if (p.d == 128) return p16 ? launch_decode_t<128, true>(p, stream) : launch_decode_t<128, false>(p, stream);
   return p16 ? launch_decode_t<64, true>(p, stream) : launch_decode_t<64, false>(p, stream);

@@ -55,9 +55,9 @@ extern "C" fattn_status fattn_decode_paged_static(const void* q, const void* kca
   if (fattn_decode_workspace_size(B, Hq, d, num_splits) > kStaticScratchBytes) return FATTN_ERR_WORKSPACE;
   void* scratch = scratch_address();
   if (!scratch) return FATTN_ERR_CUDA;
-  // Every partial the merge reads is written by this call's decode kernel
-  // (lse for every split, O for every non-empty split), so nothing in the
-  // scratch has to start at zero.
+  // The scheduling counters that must start at zero are cleared by the decode
+  // launch itself (cudaMemsetAsync on `stream`); every partial the merge reads
+  // is written by this call's decode kernel.
   return fattn_decode_paged(q, kcache, vcache, block_table, seqlens, num_splits, o, lse, B, Hq, Hkv, d, page_size,
                             max_pages_per_seq, num_pages, scale, scratch, kStaticScratchBytes, stream);
 }

@@ -37,6 +37,9 @@ cudaError_t launch_prefill_f32(const PrefillParams& p, cudaStream_t stream);
 
 struct DecodeParams {
   const void* q;
+  void* o;          // [B, Hq, d] bf16 output
+  float* lse;       // [B, Hq] or nullptr
+  int* counters;    // workspace: work counter, then one arrival counter per (sequence, KV-head group)
   const void* kcache;
   const void* vcache;
   const int32_t* block_table;
@@ -48,7 +51,10 @@ struct DecodeParams {
   int* status;
 };
 
-cudaError_t launch_decode_partials(const DecodeParams& p, cudaStream_t stream);
+// Split-KV decode with the merge fused in (one launch, after a memset of the counters).
+cudaError_t launch_decode(const DecodeParams& p, cudaStream_t stream);
+
+int num_sms_current();
 
 struct MergeParams {
   const float* o_part;

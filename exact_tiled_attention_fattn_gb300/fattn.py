@@ -148,9 +148,10 @@ def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
 
 
 def choose_num_splits(batch: int, hkv: int, max_pages_per_seq: int, num_sms: int | None = None,
-                      chunk_pages: int = 32) -> int:
+                      chunk_pages: int = 128) -> int:
     """A split count that cuts contexts into ~``chunk_pages``-page chunks and gives at
-    least two thread blocks per SM over the batch."""
+    least two work items per SM over the batch. Larger chunks amortise each item's
+    fixed cost (Q load, pipeline fill, partial write); smaller ones balance better."""
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     by_chunk = -(-max_pages_per_seq // chunk_pages)

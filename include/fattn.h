@@ -89,8 +89,8 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
 /*
  * fattn_decode_workspace_size — bytes of scratch fattn_decode_paged needs:
  * the per-split partials lse_part [B, Hq, S] fp32 and o_part [B, Hq, S, d]
- * fp32 (S = num_splits), each region 256-byte aligned. Returns 0 for
- * non-positive arguments.
+ * fp32 (S = num_splits), then 1 + B * Hq int32 work-scheduling counters, each
+ * region 256-byte aligned. Returns 0 for non-positive arguments.
  */
 size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits);
 
@@ -114,9 +114,11 @@ size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits);
  *   the end of the sequence.
  * o [B, Hq, d] bf16, lse [B, Hq] fp32 (lse may be NULL).
  * workspace: device scratch of at least fattn_decode_workspace_size(B, Hq, d,
- *   S) bytes, 256-byte aligned; after the call it holds the partials
- *   (lse_part first, then o_part; each o_part row divided by its own l, and
- *   lse_part = -inf for an empty split).
+ *   S) bytes, 256-byte aligned; its contents on entry do not matter (the call
+ *   zeroes its counters with cudaMemsetAsync on `stream`). After the call it
+ *   holds the partials (lse_part first, then o_part; each o_part row divided
+ *   by its own l, and lse_part = -inf for an empty split). The partials are
+ *   merged into o and lse inside the same kernel launch.
  * Errors: INVALID_ARG (null/misaligned pointers, non-positive sizes,
  *   Hq % Hkv != 0, non-finite scale), UNSUPPORTED (d not in {64, 128}),
  *   WORKSPACE (workspace NULL or too small). A block-table entry outside
@@ -165,10 +167,11 @@ fattn_status fattn_merge_partials(const float* o_part, const float* lse_part, vo
  * workspace. The first call on a device (with that device current) looks up
  * the scratch's device address with cudaGetSymbolAddress and caches it; make
  * that first call before any stream capture on that device. All calls share
- * the one scratch array, which keeps the last call's contents (every partial
- * a call reads back is written by that same call, so nothing needs clearing):
- * calls that overlap on the GPU — on different streams, or from different
- * host threads — race on it and must be serialised by the caller.
+ * the one scratch array, which keeps the last call's contents; each call
+ * zeroes the counters it uses (cudaMemsetAsync on `stream`) and reads back
+ * only partials it wrote itself. Calls that overlap on the GPU — on different
+ * streams, or from different host threads — race on the array and must be
+ * serialised by the caller.
  * Errors: those of fattn_decode_paged; FATTN_ERR_WORKSPACE when the partials
  * (fattn_decode_workspace_size(B, Hq, d, num_splits) bytes) exceed the
  * scratch; FATTN_ERR_CUDA if the scratch address cannot be obtained.

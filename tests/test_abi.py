@@ -100,7 +100,7 @@ def test_decode_validation(lib):
 def test_workspace_size_arithmetic(lib):
     B, Hq, d, S = 8, 32, 128, 64
     rows = B * Hq * S
-    expect = (rows * 4 + 255) // 256 * 256 + (rows * d * 4 + 255) // 256 * 256
+    expect = (rows * 4 + 255) // 256 * 256 + (rows * d * 4 + 255) // 256 * 256 + ((1 + B * Hq) * 4 + 255) // 256 * 256
     assert lib.fattn_decode_workspace_size(B, Hq, d, S) == expect
     assert lib.fattn_decode_workspace_size(0, Hq, d, S) == 0
     assert lib.fattn_decode_workspace_size(B, Hq, d, 0) == 0
