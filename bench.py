@@ -202,7 +202,7 @@ def main():
     dq, dk, dv = dec.q.to(dev), dec.kcache.to(dev), dec.vcache.to(dev)
     dbt, dsl = dec.block_table.to(dev), dec.seqlens.to(dev)
     S = args.num_splits or fattn.choose_num_splits(dec.batch, dec.hkv, dec.max_pages_per_seq)
-    ws = torch.empty(fattn.decode_workspace_size(dec.batch, dec.hq, dec.d, S), dtype=torch.uint8, device=dev)
+    ws = torch.zeros(fattn.decode_workspace_size(dec.batch, dec.hq, dec.d, S), dtype=torch.uint8, device=dev)
     do = torch.empty_like(dq)
     dlse = torch.empty((dec.batch, dec.hq), dtype=torch.float32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)

@@ -342,7 +342,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(const DecodeParams 
     __syncthreads();
     const int item = s_item;
     __syncthreads();
-    if (item >= total) break;
+    if (item < 0 || item >= total) break;  // (a negative index cannot come from a zeroed counter)
     // highest split first: the long sequences' far chunks start early, empty items go fast
     const int split = p.num_splits - 1 - item / groups;
     const int g = item - (item / groups) * groups;

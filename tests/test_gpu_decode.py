@@ -23,7 +23,7 @@ def _dev(x):
 
 def _decode(fa, x, S, dev=None):
     q, kc, vc, bt, sl = dev if dev is not None else _dev(x)
-    ws = torch.empty(fa.decode_workspace_size(x.batch, x.hq, x.d, S), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(fa.decode_workspace_size(x.batch, x.hq, x.d, S), dtype=torch.uint8, device="cuda")
     o, lse = fa.decode_paged(q, kc, vc, bt, sl, S, scale=x.scale, workspace=ws)
     st = fa.debug_read_status()
     return o, lse, ws, st
@@ -144,3 +144,15 @@ def test_merge_partials(fa, out_dtype, d):
     fin = np.isfinite(lse_ref)
     assert np.array_equal(np.isfinite(lg), fin)
     assert np.max(np.abs(lg[fin] - lse_ref[fin])) <= 1e-5
+
+
+def test_workspace_reused_across_calls(fa):
+    """Each call leaves the workspace counters at zero, so one buffer serves many calls."""
+    ws = torch.zeros(fa.decode_workspace_size(3, 8, 128, 64), dtype=torch.uint8, device="cuda")
+    for seed, S in [(70, 64), (71, 5), (72, 64), (73, 1), (74, 17)]:
+        x = inputs.decode_paged(seed, 3, 8, 2, 128, 16, (1, 3000), 3072, spare_pages=2)
+        q, kc, vc, bt, sl = _dev(x)
+        o, lse = fa.decode_paged(q, kc, vc, bt, sl, S, scale=x.scale, workspace=ws)
+        assert fa.debug_read_status() == 0
+        o_ref, lse_ref = orc.decode_paged(x.q, x.kcache, x.vcache, x.block_table, x.seqlens, x.scale)
+        check(o, lse, o_ref, lse_ref, what=f"reuse seed {seed} S {S}")
