@@ -49,6 +49,32 @@ def parse():
     return ap.parse_args()
 
 
+KERNEL_SOURCES = {
+    "prefill_tc_kernel<128>": ["prefill_tc.cu", "sm100_primitives.cuh", "device_common.cuh", "fattn_internal.h"],
+    "decode_kernel<128, page16>": ["decode.cu", "device_common.cuh", "fattn_internal.h"],
+}
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from profiles/dram_traffic.md, or None when the
+    kernel's sources changed since that capture (or none was recorded)."""
+    import hashlib
+    csrc = os.path.join(ROOT, "exact_tiled_attention_fattn_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.md")) as fh:
+            for line in fh:
+                cells = [c.strip() for c in line.strip().strip("|").split("|")]
+                if len(cells) == 3 and cells[0] == kernel and cells[2] == h.hexdigest()[:16]:
+                    return float(cells[1])
+    except OSError:
+        pass
+    return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -356,11 +382,12 @@ def main():
                    "parallelism": f"replicas x{world}", "num_splits": S,
                    "l2": "flushed (256 MB write) before every timed launch"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
-                     "frac": tflops / peak_t, "traffic": None,
+                     "frac": tflops / peak_t, "traffic": recorded_traffic("prefill_tc_kernel<128>"),
                      "peak_source": f"{peak_src} bf16_tflops (burst)", "kernel": "prefill_tc_kernel<128>"},
         "decode": {"value": world * gbs, "unit": "GB/s", "ms": t_dec, "kv_bytes": kv_bytes,
                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_b, "unit": "GB/s",
-                                "frac": gbs / peak_b, "traffic": None, "peak_source": f"{peak_src} hbm_gbs"}},
+                                "frac": gbs / peak_b, "traffic": recorded_traffic("decode_kernel<128, page16>"),
+                                "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel<128, page16>"}},
         "prefill_ms": t_pre,
         "e2e": e2e,
         "cpu_baseline": cpu,
