@@ -19,6 +19,9 @@ Sources (three web pages on one subject):
             statistics l and m).
   [CUDA-OPS] "Attention" CUDA operations guide (rightnowai.co): K/V heads shared
             by several Q heads (GQA/MQA); non-contiguous (paged) KV allocation.
+  [FA-PAPER] "Block-sparse FlashAttention": a fixed mask over blocks; every
+            block that is zero in the mask is skipped, i.e. its scores are
+            excluded from the softmax (an approximation of dense attention).
 
 Everything is computed in float64 from inputs that the caller widens exactly
 (bf16 and fp32 values are representable in fp64). The primary mode is the plain
@@ -50,6 +53,8 @@ __all__ = [
     "attention_weights",
     "attn_fwd",
     "attn_fwd_rows",
+    "attn_fwd_block_sparse",
+    "block_sparse_allowed",
     "softmax_row_blocked",
     "attention_blocked",
     "attention_blocked_normalised",
@@ -104,12 +109,13 @@ def attention_weights(q, k, scale: float, causal: bool = False, rows=None) -> np
     return np.where(l[:, None] > 0, w / np.where(l > 0, l, 1.0)[:, None], 0.0)
 
 
-def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None):
+def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None, allowed=None):
     """Exact attention for one head by the definition, fp64.
 
     q [Nq, d], k [Nk, d], v [Nk, dv]. Returns (O [r, dv], lse [r]) for the
     requested query rows (all by default), lse = m + ln(l) of the scaled,
-    masked scores (natural log).
+    masked scores (natural log). ``allowed`` (bool [Nq, Nk]) further restricts
+    which keys each query sees (M = -inf where it is False).
     """
     q = _f64(q)
     k = _f64(k)
@@ -120,6 +126,8 @@ def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None)
         return np.zeros((len(rows), v.shape[-1])), np.full(len(rows), -np.inf)
     s = scale * (q[rows] @ k.T)
     ok = _allowed(rows, nk, nq, causal)
+    if allowed is not None:
+        ok = ok & np.asarray(allowed, dtype=bool)[rows]
     s = np.where(ok, s, -np.inf)
     m = s.max(axis=1)                                  # running-max target m
     finite = np.isfinite(m)
@@ -198,6 +206,49 @@ def attn_fwd_rows(q, k, v, scale: float, causal: bool, samples, cu_seqlens=None)
             a, e = starts[b], starts[b + 1]
             qh, kh, vh = q[a:e, h], k[a:e, h // g], v[a:e, h // g]
         o[idx], lse[idx] = attention_definition(qh, kh, vh, scale, causal, rows=rows)
+    return o, lse
+
+
+def block_sparse_allowed(block_mask_2d, nq: int, nk: int, block: int) -> np.ndarray:
+    """Expand a [ceil(nq/block), ceil(nk/block)] block mask to a key-visibility
+    matrix [nq, nk]: key j is visible to query i iff block (i // block, j // block)
+    is non-zero ("Block-sparse FlashAttention": zero blocks are skipped)."""
+    bm = np.asarray(block_mask_2d) != 0
+    i = np.arange(nq) // block
+    j = np.arange(nk) // block
+    return bm[i[:, None], j[None, :]]
+
+
+def attn_fwd_block_sparse(q, k, v, scale: float, causal: bool, block_mask, block: int, rows=None):
+    """Dense-layout prefill restricted by a block mask.
+
+    q [B, N, Hq, d], k/v [B, N, Hkv, d]; block_mask [Hm, ceil(N/block),
+    ceil(N/block)] with Hm = 1 (shared) or Hq (per query head). Visible keys are
+    those the causal rule allows in a non-zero block; a row with none has O = 0,
+    lse = -inf. Returns O [B, N, Hq, d], lse [B, Hq, N] (or, with ``rows`` as an
+    int array [n, 3] of (b, h, i), O [n, d] and lse [n]).
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    bm = np.asarray(block_mask)
+    B, N, Hq, _ = q.shape
+    g = Hq // k.shape[2]
+    if rows is None:
+        o = np.zeros(q.shape[:3] + (v.shape[-1],))
+        lse = np.zeros((B, Hq, N))
+        for h in range(Hq):
+            allow = block_sparse_allowed(bm[h % bm.shape[0]], N, N, block)
+            for b in range(B):
+                o[b, :, h], lse[b, h] = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g],
+                                                             scale, causal, allowed=allow)
+        return o, lse
+    rows = np.asarray(rows, dtype=np.int64)
+    o = np.zeros((len(rows), v.shape[-1]))
+    lse = np.zeros(len(rows))
+    for n, (b, h, i) in enumerate(rows):
+        allow = block_sparse_allowed(bm[h % bm.shape[0]], N, N, block)
+        ob, lb = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
+                                      rows=np.array([i]), allowed=allow)
+        o[n], lse[n] = ob[0], lb[0]
     return o, lse
 
 

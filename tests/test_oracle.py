@@ -360,3 +360,46 @@ def test_decode_partials_merge_to_decode(S):
     o, lse = orc.merge_partials(lp, op)
     assert np.max(np.abs(o - o_ref)) <= 1e-12
     assert np.max(np.abs(lse - lse_ref)) <= 1e-12
+
+
+# ---------------------------------------------------------------- block-sparse ----
+def test_block_sparse_vs_python_loops():
+    """'Block-sparse FlashAttention': keys in zero blocks take no part in the softmax."""
+    rng = np.random.default_rng(20)
+    B, N, H, d, blk = 1, 11, 2, 4, 3
+    q, k, v = _rand(rng, B, N, H, d), _rand(rng, B, N, H, d), _rand(rng, B, N, H, d)
+    nb = -(-N // blk)
+    bm = rng.integers(0, 2, size=(H, nb, nb)).astype(np.uint8)
+    bm[:, :, 0] = 1                                   # every row keeps at least one block
+    for causal in (False, True):
+        o, lse = orc.attn_fwd_block_sparse(q, k, v, 0.5, causal, bm, blk)
+        for h in range(H):
+            for i in range(N):
+                keys = [j for j in range(N) if bm[h, i // blk, j // blk] and (not causal or j <= i)]
+                s = [0.5 * float(q[0, i, h] @ k[0, j, h]) for j in keys]
+                mx = max(s)
+                w = [math.exp(x - mx) for x in s]
+                tot = sum(w)
+                ref = sum(wi * v[0, j, h] for wi, j in zip(w, keys)) / tot
+                assert np.max(np.abs(o[0, i, h] - ref)) <= 1e-13
+                assert abs(lse[0, h, i] - (mx + math.log(tot))) <= 1e-13
+
+
+def test_block_sparse_all_ones_is_dense_and_empty_rows():
+    rng = np.random.default_rng(21)
+    B, N, Hq, Hkv, d, blk = 2, 10, 4, 2, 8, 4
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    nb = -(-N // blk)
+    for causal in (False, True):
+        o1, l1 = orc.attn_fwd_block_sparse(q, k, v, 0.3, causal, np.ones((1, nb, nb), np.uint8), blk)
+        o2, l2 = orc.attn_fwd(q, k, v, 0.3, causal)
+        assert np.max(np.abs(o1 - o2)) <= 1e-14 and np.max(np.abs(l1 - l2)) <= 1e-14
+    bm = np.ones((1, nb, nb), np.uint8)
+    bm[0, 1, :] = 0                                   # query block 1 sees nothing
+    o, lse = orc.attn_fwd_block_sparse(q, k, v, 0.3, False, bm, blk)
+    assert np.all(o[:, blk:2 * blk] == 0) and np.all(np.isneginf(lse[:, :, blk:2 * blk]))
+    smp = np.array([[1, 3, 9], [0, 0, 5], [1, 2, 0]])
+    os_, ls_ = orc.attn_fwd_block_sparse(q, k, v, 0.3, False, bm, blk, rows=smp)
+    for n, (b, h, i) in enumerate(smp):
+        assert np.array_equal(os_[n], o[b, i, h]) or np.max(np.abs(os_[n] - o[b, i, h])) <= 1e-14
+        assert (np.isneginf(ls_[n]) and np.isneginf(lse[b, h, i])) or abs(ls_[n] - lse[b, h, i]) <= 1e-14
