@@ -109,6 +109,8 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
 
   int err = 0;
   PrefillParams p;
+  p.block_mask = nullptr;
+  p.mask_heads = 1;
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = cu_seqlens;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
   p.causal = causal ? 1 : 0; p.scale = scale;
@@ -128,6 +130,40 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
     e = launch_prefill_tc(p, tq, tk, tv, sms, stream);
   }
   return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                               int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                                               const uint8_t* block_mask, int mask_heads, cudaStream_t stream) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !block_mask) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || (mask_heads != 1 && mask_heads != Hq)) return FATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  static_assert(FATTN_SPARSE_MAX_BLOCKS == kSparseMaxBlocks, "mask row limit");
+  if ((N + FATTN_SPARSE_BLOCK - 1) / FATTN_SPARSE_BLOCK > FATTN_SPARSE_MAX_BLOCKS) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * N;
+  if (rows > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+
+  int err = 0;
+  PrefillParams p;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
+  p.causal = causal ? 1 : 0; p.scale = scale;
+  p.block_mask = block_mask;
+  p.mask_heads = mask_heads;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
+      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+    return FATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }

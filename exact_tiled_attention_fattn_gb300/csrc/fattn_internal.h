@@ -25,7 +25,14 @@ struct PrefillParams {
   int causal;
   float scale;
   int* status;                // device status word
+  // block-sparse variant only: uint8 [mask_heads][nb][nb], nb = ceil(N / 128);
+  // block (qb, kb) = 0 hides keys [128 kb, 128 kb + 128) from queries [128 qb, 128 qb + 128)
+  const uint8_t* block_mask;  // nullptr = dense
+  int mask_heads;             // 1 (shared by all heads) or Hq
 };
+
+// Longest mask row (blocks) the block-sparse kernel holds in shared memory.
+constexpr int kSparseMaxBlocks = 2048;
 
 // Tensor-core prefill (bf16 in, fp32 accumulate, bf16 out). Tensor maps are
 // encoded by the caller over the packed [rows, H, d] views of q, k and v.

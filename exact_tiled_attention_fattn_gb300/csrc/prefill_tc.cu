@@ -10,8 +10,9 @@
 //               O_A += P_A(j-1) V_{j-1}, S_A = Q_A K_j^T, O_B += P_B(j-1) V_{j-1},
 //               S_B = Q_B K_j^T, so that while one softmax warpgroup works on its
 //               scores the tensor core runs the other tile's two products.
-//   warps 2-3   idle (they complete the first warpgroup, which gives registers
-//               to the softmax warpgroups with setmaxnreg).
+//   warps 2-3   complete the first warpgroup, which gives registers to the
+//               softmax warpgroups with setmaxnreg; in the block-sparse variant
+//               warp 2 reads the block mask ahead of the other roles.
 //   warps 4-7   softmax of tile A, warps 8-11 softmax of tile B: each thread owns
 //               one query row (TMEM lane); it loads its 128 scores, masks (causal
 //               diagonal, sequence end), keeps the running max m and sum l in
@@ -23,6 +24,13 @@
 // and l use the same m), which makes the O rescale rare.
 // Causal tiles above the diagonal are never loaded or computed ("tiles above
 // the diagonal are never touched"). S and P never leave the SM.
+// Block-sparse variant ("Block-sparse FlashAttention": zero blocks of a fixed
+// block mask are skipped): with 128 x 128 blocks, a tile visits only the K/V
+// blocks its mask row keeps; warp 2 turns the item's two mask rows into bit
+// words in a shared-memory ring, the producer and the MMA warp walk the union
+// of the two tiles' kept blocks in the same interleaved order, each softmax
+// warpgroup walks its own row, and a tile whose rows keep no block writes
+// O = 0, lse = -inf.
 //
 // P_X aliases S_X: S_X(j) is issued right after O_X += P_X(j-1) V by the same
 // thread, and tcgen05.mma operations issued by one thread execute in order, so
@@ -57,10 +65,26 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 88;
 constexpr int kRegsSoftmax = 208;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+// The block-sparse variant's walks over the mask bits need more registers in
+// the producer/MMA/mask warpgroup: 128 * 104 + 256 * 200 = 64512.
+constexpr int kRegsControlSparse = 104;
+constexpr int kRegsSoftmaxSparse = 200;
+static_assert(128 * kRegsControlSparse + 256 * kRegsSoftmaxSparse <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
 constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exceed it by <= 2^8
+
+// Block-mask ring (block-sparse variant): warp 2 reads the two mask rows of
+// each item into bit words (bit j of row t: tile t keeps K/V block j, already
+// clipped to the blocks the tile visits), with the kept-block counts and the
+// last block either tile keeps. Producer, MMA issuer and softmax warps walk
+// the bits from shared memory, so no mask load sits on their paths.
+constexpr int kMaskSlots = 4;
+constexpr int kMaskWords = 64;                        // up to 2048 blocks per row
+constexpr int kMaskSlotBytes = 2 * kMaskWords * 4 + 16;
+constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8 softmax warps
+static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
 template <int D>
 struct TcLayout {
@@ -71,12 +95,13 @@ struct TcLayout {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-  static constexpr int kNumBars = 17;
+  static constexpr int kNumBars = 17 + 2 * kMaskSlots;
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
+  static constexpr int kOffMask = kOffAbort + 8;  // block-mask ring (block-sparse variant)
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would block in tcgen05.alloc) never shares the SM
-  static constexpr int kUsed = kOffAbort + 8 + 1024;
+  static constexpr int kUsed = kOffMask + kMaskSlots * kMaskSlotBytes + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
   // TMEM columns: fp32 scores S_A, S_B (P_X in bf16 over their first 64 columns), fp32 O_A, O_B.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
@@ -87,7 +112,8 @@ struct TcLayout {
 // barrier slots
 enum : int {
   kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8,
-  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16
+  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16,
+  kBarMaskFull = 17, kBarMaskEmpty = 17 + kMaskSlots
 };
 
 struct Item {
@@ -165,6 +191,30 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, const Schedu
   return x;
 }
 
+// Walks the kept blocks of one mask row (sel = 1 << t) or of the union of both
+// rows (sel = 3) in increasing order. The current word of each row is held in
+// registers, so a step costs a find-first-set; shared memory is read once per
+// 32 blocks. Bits past a row's n[t] are zero, so the walk ends by itself.
+struct BitWalk {
+  const uint32_t* w;
+  int sel, nw, wi, bit;
+  uint32_t u0, u1, rem;
+  __device__ __forceinline__ BitWalk(const uint32_t* words, int sel_, int end)
+      : w(words), sel(sel_), nw((end + 31) >> 5), wi(-1), bit(0), u0(0), u1(0), rem(0) {}
+  __device__ __forceinline__ int next() {  // next kept block, or -1
+    while (rem == 0) {
+      if (++wi >= nw) return -1;
+      u0 = (sel & 1) ? w[wi] : 0u;
+      u1 = (sel & 2) ? w[kMaskWords + wi] : 0u;
+      rem = u0 | u1;
+    }
+    bit = __ffs(rem) - 1;
+    rem &= rem - 1;
+    return wi * 32 + bit;
+  }
+  __device__ __forceinline__ bool kept(int t) const { return ((t ? u1 : u0) >> bit) & 1u; }
+};
+
 // Drain wait: bounded, ignores the abort flag (used on the way out).
 __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
@@ -207,7 +257,7 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
   return d;
 }
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -217,11 +267,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sb = smem_u32(smem);
   auto bar = [&](int i) -> uint32_t { return sb + Lay::kOffBar + 8 * i; };
   volatile int* abort = reinterpret_cast<volatile int*>(smem + Lay::kOffAbort);
+  // u-th item's block-mask slot: bit words of rows 0 and 1, then {cnt0, cnt1, last}
+  auto mask_slot = [&](uint32_t u) -> const uint32_t* {
+    return reinterpret_cast<const uint32_t*>(smem + Lay::kOffMask + (u % kMaskSlots) * kMaskSlotBytes);
+  };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4 : 1);
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4
+                        : (i >= kBarMaskEmpty)                  ? kMaskConsumers
+                                                                : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -243,11 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsControl));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsControlSparse : kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t nq = 0, nk = 0, nv = 0;
+      uint32_t nq = 0, nk = 0, nv = 0, nm = 0;
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
       for (int k = 0;; ++k) {
         const int it = item_index(sch, k);
@@ -256,6 +312,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!x.valid) continue;
         const int hkv = x.h / G;
         const int n = max(x.n[0], x.n[1]);
+        const uint32_t* mw = nullptr;
+        if constexpr (kSparse) {
+          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, kWaitLimitNs))
+            break;
+          mw = mask_slot(nm);
+          if ((int)mw[2 * kMaskWords + 2] < 0) {  // neither tile keeps a block: Q is not needed
+            mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
+            ++nm;
+            continue;
+          }
+        }
         if (!mbar_wait(bar(kBarQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
         mbar_arrive_expect_tx(bar(kBarQFull), 2 * Lay::kQBytes);
 #pragma unroll
@@ -287,10 +354,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nv;
           return true;
         };
-        // the order the MMA warp consumes them: K0 K1 V0 K2 V1 K3 V2 ...
-        bool ok = load_k(0) && (n < 2 || load_k(1)) && load_v(0);
-        for (int j = 2; ok && j < n; ++j) ok = load_k(j) && load_v(j - 1);
-        if (ok && n > 1) ok = load_v(n - 1);
+        // the order the MMA warp consumes them: K0 K1 V0 K2 V1 K3 V2 ... (over the
+        // blocks either tile visits)
+        bool ok = true;
+        int prev = -1;
+        if constexpr (kSparse) {
+          BitWalk walk(mw, 3, n);
+          for (int j = walk.next(); ok && j >= 0; j = walk.next()) {
+            ok = load_k(j) && (prev < 0 || load_v(prev));
+            prev = j;
+          }
+          mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
+          ++nm;
+        } else {
+          for (int j = 0; ok && j < n; ++j) {
+            ok = load_k(j) && (prev < 0 || load_v(prev));
+            prev = j;
+          }
+        }
+        if (ok && prev >= 0) ok = load_v(prev);
         if (!ok) break;
       }
       // no copy may land after the CTA is gone: wait for the last armed phase of each barrier
@@ -341,11 +423,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       bool ok = true;
+      uint32_t nm = 0;
       for (int k = 0; ok; ++k) {
         const int it = item_index(sch, k);
         if (it < 0) break;
         const Item x = decode_item(p, sch, it);
         if (!x.valid) continue;
+        if constexpr (kSparse) {
+          // walk the blocks either tile keeps: per block j, O_t += P_t(prev) V_prev for each tile
+          // that kept the previous block, then S_t = Q_t K_j^T for each tile that keeps j
+          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, kWaitLimitNs))
+            break;
+          const uint32_t* mw = mask_slot(nm);
+          const int cnt[2] = {(int)mw[2 * kMaskWords], (int)mw[2 * kMaskWords + 1]};
+          const int last = (int)mw[2 * kMaskWords + 2];
+          if (last < 0) {  // the producer loads no Q for this item
+            mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
+            ++nm;
+            continue;
+          }
+          if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
+          ++nq;
+          tc_fence_after();
+          const int n = max(x.n[0], x.n[1]);
+          int done0 = 0, done1 = 0;          // P V products issued per tile
+          bool had0 = false, had1 = false;    // tile kept the previous union block
+          bool first = true;
+          BitWalk walk(mw, 3, n);
+          for (int j = walk.next(); j >= 0; j = walk.next()) {
+            const bool a0 = walk.kept(0), a1 = walk.kept(1);
+            const uint32_t kst = nk & 1, vst = nv & 1;
+            if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
+                (!first && !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs))) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            if (had0) {
+              if (!issue_pv(0, vst, done0 > 0)) { ok = false; break; }
+              if (++done0 == cnt[0]) mma_commit(bar(kBarOFull + 0));
+            }
+            if (a0) issue_s(0, kst);
+            if (had1) {
+              if (!issue_pv(1, vst, done1 > 0)) { ok = false; break; }
+              if (++done1 == cnt[1]) mma_commit(bar(kBarOFull + 1));
+            }
+            if (a1) issue_s(1, kst);
+            had0 = a0;
+            had1 = a1;
+            mma_commit(bar(kBarKEmpty + kst));
+            ++nk;
+            if (!first) {
+              mma_commit(bar(kBarVEmpty + vst));
+              ++nv;
+            }
+            if (j == last) mma_commit(bar(kBarQEmpty));
+            first = false;
+          }
+          if (!ok) break;
+          const uint32_t vst = nv & 1;
+          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
+          tc_fence_after();
+          if (had0) {
+            if (!issue_pv(0, vst, done0 > 0)) break;
+            mma_commit(bar(kBarOFull + 0));
+          }
+          if (had1) {
+            if (!issue_pv(1, vst, done1 > 0)) break;
+            mma_commit(bar(kBarOFull + 1));
+          }
+          mma_commit(bar(kBarVEmpty + vst));
+          ++nv;
+          mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
+          ++nm;
+          continue;
+        }
         const int nA = x.n[0], nB = x.n[1];
         const int n = max(nA, nB);
         if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
@@ -408,9 +560,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(kBarMmaDone));
       mbar_drain(bar(kBarMmaDone), 0);
     }
+  } else if (kSparse && warp == 2) {
+    // ------------------------------------------------------------ block-mask reader
+    // Per item: lane i tests blocks 32 w + i of both mask rows, a ballot packs
+    // them into word w; blocks at or past n[t] (causal skip, sequence end) are 0.
+    const int nb = (p.N + BN - 1) / BN;
+    uint32_t nm = 0;
+    for (int k = 0;; ++k) {
+      const int it = item_index(sch, k);
+      if (it < 0) break;
+      const Item x = decode_item(p, sch, it);
+      if (!x.valid) continue;
+      if (!warp_wait(bar(kBarMaskEmpty + nm % kMaskSlots), ((nm / kMaskSlots) & 1) ^ 1, abort, p.status)) break;
+      uint32_t* w = reinterpret_cast<uint32_t*>(smem + Lay::kOffMask + (nm % kMaskSlots) * kMaskSlotBytes);
+      const int nw = (max(x.n[0], x.n[1]) + 31) >> 5;   // <= kMaskWords: nb <= kSparseMaxBlocks
+      int cnt[2] = {0, 0}, last = -1;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const uint8_t* mrow = p.block_mask + ((size_t)(x.h % p.mask_heads) * nb + (x.base / BM + t)) * nb;
+        for (int w0 = 0; w0 < nw; w0 += 4) {
+          uint32_t v[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int j = (w0 + i) * 32 + lane;
+            v[i] = j < x.n[t] ? __ldg(mrow + j) : 0u;      // j < n[t] <= nb: inside row t
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t bits = __ballot_sync(0xffffffffu, v[i] != 0u);
+            if (w0 + i < nw) {
+              if (lane == 0) w[t * kMaskWords + w0 + i] = bits;
+              cnt[t] += __popc(bits);
+              if (bits) last = max(last, (w0 + i) * 32 + 31 - __clz(bits));
+            }
+          }
+        }
+      }
+      if (lane == 0) {
+        w[2 * kMaskWords] = (uint32_t)cnt[0];
+        w[2 * kMaskWords + 1] = (uint32_t)cnt[1];
+        w[2 * kMaskWords + 2] = (uint32_t)last;
+        mbar_arrive(bar(kBarMaskFull + nm % kMaskSlots));  // release: the words above are visible
+      }
+      __syncwarp();
+      ++nm;
+    }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsSoftmaxSparse : kRegsSoftmax));
     // ------------------------------------------------------------ softmax (tile t)
     const int t = (warp - 4) >> 2;           // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may touch
@@ -422,16 +619,53 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool neg = sl2 < 0.f;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t ns = 0, no = 0;                 // S_t and O_t completions seen
+    uint32_t nm = 0;                         // block-mask slots consumed
     bool ok = true;
     for (int k = 0; ok; ++k) {
       const int it = item_index(sch, k);
       if (it < 0) break;
       const Item x = decode_item(p, sch, it);
-      if (!x.valid || x.n[t] == 0) continue;
+      if (!x.valid) continue;
+      const uint32_t* mw = nullptr;
+      int kept_blocks = x.n[t];
+      if constexpr (kSparse) {
+        const uint32_t mb = bar(kBarMaskFull + nm % kMaskSlots), mp = (nm / kMaskSlots) & 1;
+        if (!warp_wait(mb, mp, abort, p.status)) break;
+        mbar_try_wait(mb, mp);  // completed: this lane's own acquire of the mask words
+        mw = mask_slot(nm);
+        kept_blocks = (int)mw[2 * kMaskWords + t];
+      }
+      // the mask words stay in use until every consumer of the slot releases it
+      auto release_mask = [&]() {
+        if constexpr (kSparse) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
+          ++nm;
+        }
+      };
+      if (x.n[t] == 0) {
+        release_mask();
+        continue;
+      }
       const int row = x.base + t * BM + r;
       const int lim = p.causal ? min(row + 1, x.L) : x.L;  // keys < lim are visible
+      if constexpr (kSparse) {  // a tile that keeps no block: O = 0, lse = -inf
+        if (kept_blocks == 0) {
+          release_mask();
+          if (row < x.L) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) +
+                                                  ((size_t)(x.row0 + row) * p.Hq + x.h) * D);
+#pragma unroll
+            for (int e = 0; e < D / 8; ++e) dst[e] = make_uint4(0, 0, 0, 0);
+            if (p.lse) p.lse[((size_t)x.b * p.Hq + x.h) * p.N + row] = -CUDART_INF_F;
+          }
+          continue;
+        }
+      }
       float m = -CUDART_INF_F, l = 0.f;
-      for (int j = 0; j < x.n[t]; ++j) {
+      bool first = true;
+      BitWalk walk(mw, 1 << t, x.n[t]);
+      for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < x.n[t]; j = kSparse ? walk.next() : j + 1) {
         if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status)) {
           ok = false;
           break;
@@ -502,7 +736,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * alpha + sum;
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O_t += P_t(j-1) V has completed (covered by the commit of S_t(j)).
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
@@ -514,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         m = m_new;
+        first = false;
         tmem_st64(s_col, pk);
         tmem_st_wait();
         tc_fence_before();
@@ -521,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kBarPFull + t));
       }
       if (!ok) break;
+      release_mask();
       // epilogue: O / l in bf16 and the row's logsumexp
       if (!warp_wait(bar(kBarOFull + t), no & 1, abort, p.status)) {
         ok = false;
@@ -563,11 +799,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kSparse>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      int num_sms, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<D>;
+  auto kern = prefill_tc_kernel<D, kSparse>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   const long long pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
@@ -582,8 +818,12 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
-  if (p.d == 128) return launch_t<128>(p, tq, tk, tv, num_sms, stream);
-  return launch_t<64>(p, tq, tk, tv, num_sms, stream);
+  if (p.block_mask) {
+    if (p.d == 128) return launch_t<128, true>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, true>(p, tq, tk, tv, num_sms, stream);
+  }
+  if (p.d == 128) return launch_t<128, false>(p, tq, tk, tv, num_sms, stream);
+  return launch_t<64, false>(p, tq, tk, tv, num_sms, stream);
 }
 
 }  // namespace fattn

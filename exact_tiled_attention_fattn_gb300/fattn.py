@@ -31,6 +31,7 @@ FATTN_FP32 = 1
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 SIGNATURES = {
     "fattn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _i, _vp]),
+    "fattn_fwd_block_sparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
     "fattn_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fattn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz,
                                 _vp]),
@@ -102,6 +103,16 @@ def _need_cuda(*ts):
             raise ValueError("all tensors must be contiguous")
 
 
+def _expect(t, shape, name, dtype=None):
+    """Shape (and dtype) check of an argument the library will read or write in full."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+
+
 def fwd(q, k, v, causal: bool = False, scale: float | None = None, cu_seqlens=None, max_seqlen: int | None = None,
         out=None, lse=None, want_lse: bool = True, stream=None):
     """Prefill attention. Dense q [B,N,Hq,d] / k,v [B,N,Hkv,d]; varlen q [T,Hq,d] with
@@ -119,7 +130,10 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, cu_seqlens=No
         if q.dim() != 4:
             raise ValueError("dense q must be [B, N, Hq, d]")
         B, N, Hq, _ = q.shape
+        if k.dim() != 4:
+            raise ValueError("dense k must be [B, N, Hkv, d]")
         Hkv = k.shape[2]
+        kv_shape, o_shape = (B, N, Hkv, d), (B, N, Hq, d)
         T = B * N
         lse_shape = (B, Hq, N)
     else:
@@ -128,10 +142,17 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, cu_seqlens=No
         if cu_seqlens.dtype != torch.int32:
             raise TypeError("cu_seqlens must be int32")
         T, Hq, _ = q.shape
+        if k.dim() != 3:
+            raise ValueError("varlen k must be [T, Hkv, d]")
         Hkv = k.shape[1]
+        kv_shape, o_shape = (T, Hkv, d), (T, Hq, d)
         B = cu_seqlens.numel() - 1
         N = int(max_seqlen)
         lse_shape = (Hq, T)
+    _expect(k, kv_shape, "k")
+    _expect(v, kv_shape, "v")
+    _expect(out, o_shape, "out", q.dtype)
+    _expect(lse, lse_shape, "lse", torch.float32)
     if out is None:
         out = torch.empty_like(q)
     if lse is None and want_lse:
@@ -140,6 +161,43 @@ def fwd(q, k, v, causal: bool = False, scale: float | None = None, cu_seqlens=No
                        float(scale), _ptr(cu_seqlens), T if cu_seqlens is not None else 0, _dtype_code(q.dtype),
                        ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_fwd", st)
+    return out, lse
+
+
+SPARSE_BLOCK = 128  # FATTN_SPARSE_BLOCK: rows/keys per block-mask entry
+
+
+def fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                     want_lse: bool = True, stream=None):
+    """Prefill restricted by a block mask. q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16;
+    block_mask uint8 [mask_heads, nb, nb] on the device, nb = ceil(N/128), mask_heads 1 or Hq.
+    Returns (O, lse [B,Hq,N]); rows that keep no key get O = 0, lse = -inf."""
+    lib = load_library()
+    _need_cuda(q, k, v, block_mask, out, lse)
+    if not (q.dtype == k.dtype == v.dtype == torch.bfloat16):
+        raise TypeError("block-sparse prefill takes bf16 q, k, v")
+    if block_mask.dtype != torch.uint8 or block_mask.dim() != 3:
+        raise TypeError("block_mask must be uint8 [mask_heads, nb, nb]")
+    B, N, Hq, d = q.shape
+    if k.dim() != 4:
+        raise ValueError("k must be [B, N, Hkv, d]")
+    _expect(k, (B, N, k.shape[2], d), "k")
+    _expect(v, k.shape, "v")
+    _expect(out, q.shape, "out", q.dtype)
+    _expect(lse, (B, Hq, N), "lse", torch.float32)
+    nb = -(-N // SPARSE_BLOCK)
+    if block_mask.shape[1] != nb or block_mask.shape[2] != nb:
+        raise ValueError(f"block_mask must be [mask_heads, {nb}, {nb}]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    st = lib.fattn_fwd_block_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, k.shape[2], N, d,
+                                    1 if causal else 0, float(scale), _ptr(block_mask), block_mask.shape[0],
+                                    ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_fwd_block_sparse", st)
     return out, lse
 
 
@@ -169,6 +227,13 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, num_splits: int, scale
         raise TypeError("block_table and seqlens must be int32")
     B, Hq, d = q.shape
     num_pages, page_size, Hkv, _ = kcache.shape
+    _expect(kcache, (num_pages, page_size, Hkv, d), "kcache")
+    _expect(vcache, kcache.shape, "vcache")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table must be [{B}, max_pages_per_seq]")
+    _expect(seqlens, (B,), "seqlens")
+    _expect(out, q.shape, "out", q.dtype)
+    _expect(lse, (B, Hq), "lse", torch.float32)
     maxp = block_table.shape[1]
     if scale is None:
         scale = 1.0 / math.sqrt(d)
@@ -203,6 +268,13 @@ def decode_paged_static(q, kcache, vcache, block_table, seqlens, num_splits: int
         raise TypeError("block_table and seqlens must be int32")
     B, Hq, d = q.shape
     num_pages, page_size, Hkv, _ = kcache.shape
+    _expect(kcache, (num_pages, page_size, Hkv, d), "kcache")
+    _expect(vcache, kcache.shape, "vcache")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table must be [{B}, max_pages_per_seq]")
+    _expect(seqlens, (B,), "seqlens")
+    _expect(out, q.shape, "out", q.dtype)
+    _expect(lse, (B, Hq), "lse", torch.float32)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
@@ -233,6 +305,11 @@ def merge_partials(o_part, lse_part, out_dtype=torch.bfloat16, out=None, lse=Non
     lib = load_library()
     _need_cuda(o_part, lse_part, out, lse)
     B, Hq, S, d = o_part.shape
+    _expect(lse_part, (B, Hq, S), "lse_part", torch.float32)
+    if o_part.dtype != torch.float32:
+        raise TypeError("o_part must be float32")
+    _expect(out, (B, Hq, d), "out")
+    _expect(lse, (B, Hq), "lse", torch.float32)
     if out is None:
         out = torch.empty((B, Hq, d), dtype=out_dtype, device=o_part.device)
     if lse is None and want_lse:

@@ -87,6 +87,30 @@ fattn_status fattn_fwd(const void* q, const void* k, const void* v, void* o, flo
                        fattn_dtype dtype, cudaStream_t stream);
 
 /*
+ * fattn_fwd_block_sparse — prefill restricted by a fixed block mask.
+ * [FA-PAPER] "Block-sparse FlashAttention": given a fixed mask over blocks,
+ * every tile that is zero in the mask is skipped (its scores take no part in
+ * the softmax); the causal skip of fattn_fwd is the special case.
+ *
+ * Dense layout and bf16 only: q [B, N, Hq, d], k and v [B, N, Hkv, d],
+ * o [B, N, Hq, d], lse [B, Hq, N] (lse may be NULL).
+ * block_mask: DEVICE uint8 [mask_heads, nb, nb] with nb = ceil(N /
+ *   FATTN_SPARSE_BLOCK); entry (h, i, j) != 0 keeps keys [128 j, 128 j + 128)
+ *   for queries [128 i, 128 i + 128) of query head h (mask_heads = 1: one mask
+ *   for every head; mask_heads = Hq: one per query head). With causal != 0
+ *   the causal rule applies on top. A row that keeps no key gets O = 0,
+ *   lse = -inf. Blocks that are zero are never loaded or computed.
+ * Errors: those of fattn_fwd, INVALID_ARG for a NULL block_mask or
+ *   mask_heads not in {1, Hq}, UNSUPPORTED for nb > FATTN_SPARSE_MAX_BLOCKS
+ *   (N > 262144).
+ */
+#define FATTN_SPARSE_BLOCK 128
+#define FATTN_SPARSE_MAX_BLOCKS 2048
+fattn_status fattn_fwd_block_sparse(const void* q, const void* k, const void* v, void* o, float* lse,
+                                    int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                                    const uint8_t* block_mask, int mask_heads, cudaStream_t stream);
+
+/*
  * fattn_decode_workspace_size — bytes of scratch fattn_decode_paged needs:
  * the per-split partials lse_part [B, Hq, S] fp32 and o_part [B, Hq, S, d]
  * fp32 (S = num_splits), then 1 + B * Hq int32 work-scheduling counters, each

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted(fattn.SIGNATURES), "binding signatures must mirror include/fattn.h"
     for n in names:
         assert hasattr(lib, n), n
-    assert set(names) == {"fattn_fwd", "fattn_decode_workspace_size", "fattn_decode_paged",
+    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_decode_workspace_size", "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
                           "fattn_debug_read_status"}
 
@@ -122,3 +122,16 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(fattn, "_lib", None)
     with pytest.raises(RuntimeError, match="libfattn.so not found"):
         fattn.load_library(str(tmp_path / "nope.so"))
+
+
+def test_block_sparse_validation(lib):
+    E = fattn
+    f = lambda **kw: lib.fattn_fwd_block_sparse(kw.get("q", A), A, A, A, A, kw.get("B", 1), kw.get("Hq", 4), 2,
+                                                kw.get("N", 256), kw.get("d", 128), 1, 0.1, kw.get("m", A),
+                                                kw.get("mh", 1), None)
+    assert f(m=None) == E.FATTN_ERR_INVALID_ARG
+    assert f(mh=2) == E.FATTN_ERR_INVALID_ARG          # neither 1 nor Hq
+    assert f(q=A + 8) == E.FATTN_ERR_INVALID_ARG
+    assert f(d=80) == E.FATTN_ERR_UNSUPPORTED
+    assert f(N=2048 * 128 + 1) == E.FATTN_ERR_UNSUPPORTED  # mask rows longer than 2048 blocks
+    assert f(B=0, q=None, m=None) == E.FATTN_OK          # empty problem
