@@ -7,7 +7,9 @@ One step = one pass of the whole path on one synthetic batch:
     (seed 4), 16-token pages (decode-partials kernel + merge kernel).
 ``value`` is prefill causal-adjusted TFLOP/s (4*B*Hq*N^2*d / 2 per step) summed
 over ranks; decode KV GB/s is reported beside it. Inputs are resident in HBM
-when timing starts; L2 is flushed (256 MB write) before every timed launch.
+when timing starts. Before every timed launch L2 is flushed: a 256 MB buffer
+is written, then a second 256 MB buffer is read, so the launch finds neither
+its inputs nor dirty lines (whose write-back it would otherwise pay) in L2.
 ``e2e`` repeats the step through the same public API from pinned host buffers,
 host<->device copies included.
 
@@ -43,9 +45,11 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0, help="decode splits (0 = library heuristic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sparse", action="store_true", help="skip the block-sparse prefill measurement")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--profile-once", action="store_true",
-                    help="one prefill and one decode launch on the bench workloads, then exit (for ncu)")
+                    help="one prefill, one decode and one block-sparse launch on the bench workloads, "
+                         "then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -53,6 +57,7 @@ KERNEL_SOURCES = {
     "prefill_tc_kernel<128>": ["prefill_tc.cu", "sm100_primitives.cuh", "device_common.cuh", "fattn_internal.h"],
     "decode_kernel<128, page16>": ["decode.cu", "device_common.cuh", "fattn_internal.h"],
 }
+KERNEL_SOURCES["prefill_tc_kernel<128, sparse>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 
 
 def recorded_traffic(kernel: str):
@@ -148,6 +153,60 @@ def make_workloads():
     return pre, dec
 
 
+def local_global_mask(nb: int, window: int):
+    """Block mask [1, nb, nb]: each query block keeps its `window` nearest key
+    blocks at or below the diagonal and the first block."""
+    import numpy as np
+    m = np.zeros((1, nb, nb), np.uint8)
+    for i in range(nb):
+        m[0, i, max(0, i - window + 1): i + 1] = 1
+        m[0, i, 0] = 1
+    return m
+
+
+def block_sparse_flops(mask, B: int, H: int, d: int, blk: int = 128) -> float:
+    """Causal work in the kept blocks, counted like the dense convention: a
+    block below the diagonal is blk^2 (q, k) pairs, a diagonal block blk^2 / 2."""
+    import numpy as np
+    m = np.tril(mask[0])
+    pairs = float(np.sum(m)) * blk * blk - float(np.trace(m)) * blk * blk / 2
+    return 4.0 * d * pairs * B * H
+
+
+def block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks):
+    """Block-sparse prefill on the bench's causal MHA inputs: a local (3 blocks)
+    + global (first block) mask, and the all-kept causal mask, which does the
+    dense kernel's work through the sparse path."""
+    import numpy as np
+    import torch
+    B, N, H, d = pre.q.shape
+    nb = N // 128
+    res = {"workload": f"causal MHA B={B} Hq=Hkv={H} N={N} d={d}, 128x128 blocks, one mask for all heads"}
+    for name, window in (("local3_global", 3), ("all_causal_blocks", nb)):
+        mh = local_global_mask(nb, window)
+        mt = torch.from_numpy(mh).to(q.device)
+        run = lambda: fattn.fwd_block_sparse(q, k, v, mt, causal=True, scale=pre.scale, out=o, lse=lse)
+        for _ in range(3):
+            flush()
+            run()
+        ts = []
+        for _ in range(10):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            run()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        t = statistics.median(ts)
+        fl = block_sparse_flops(mh, B, H, d)
+        tf = fl / (t * 1e-3) / 1e12
+        res[name] = {"ms": t, "kept_block_fraction": float(np.tril(mh[0]).sum()) / (nb * (nb + 1) / 2),
+                     "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"]}
+    res["local3_global"]["traffic"] = recorded_traffic("prefill_tc_kernel<128, sparse>")
+    return res
+
+
 def cpu_baseline_prefill(pre, seconds: float):
     """Time the fp64 oracle on sampled query rows of the prefill workload."""
     import numpy as np
@@ -231,7 +290,12 @@ def main():
     ws = torch.zeros(fattn.decode_workspace_size(dec.batch, dec.hq, dec.d, S), dtype=torch.uint8, device=dev)
     do = torch.empty_like(dq)
     dlse = torch.empty((dec.batch, dec.hq), dtype=torch.float32, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_w.zero_()
+        flush_r.max()
 
     def prefill():
         fattn.fwd(q, k, v, causal=True, scale=pre.scale, out=o, lse=lse)
@@ -242,6 +306,10 @@ def main():
     if args.profile_once:
         prefill()
         decode()
+        if not args.no_sparse:  # one block-sparse launch: local (3 blocks) + global mask
+            nb = pre.q.shape[1] // 128
+            mt = torch.from_numpy(local_global_mask(nb, 3)).to(dev)
+            fattn.fwd_block_sparse(q, k, v, mt, causal=True, scale=pre.scale, out=o, lse=lse)
         torch.cuda.synchronize()
         st = fattn.debug_read_status()
         print(json.dumps({"profile_once": True, "num_splits": S, "device_status": st}), flush=True)
@@ -250,9 +318,9 @@ def main():
         return
 
     for _ in range(max(3, args.warmup)):
-        flush.zero_()
+        flush()
         prefill()
-        flush.zero_()
+        flush()
         decode()
     torch.cuda.synchronize()
     assert fattn.debug_read_status() == 0
@@ -266,11 +334,11 @@ def main():
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     for s in range(args.steps):
-        flush.zero_()
+        flush()
         ev[s][0].record(stream)
         prefill()
         ev[s][1].record(stream)
-        flush.zero_()
+        flush()
         ev[s][2].record(stream)
         decode()
         ev[s][3].record(stream)
@@ -279,7 +347,7 @@ def main():
         dist.barrier()
     t_wall = time.perf_counter() - t_wall
     clocks = sampler.stop()
-    launches = 3 * args.steps
+    launches = 2 * args.steps  # per step: prefill_tc_kernel, decode_kernel (+ the counter memset, a driver op)
     status = fattn.debug_read_status()
 
     pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
@@ -354,6 +422,8 @@ def main():
                "prefill_ms": tp, "decode_ms": td,
                "decode": {"value": world * kv_bytes / (td * 1e-3) / 1e9, "unit": "GB/s"}}
 
+    sparse = None if args.no_sparse else block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pre, args.cpu_seconds)
@@ -380,7 +450,7 @@ def main():
         "config": {"workload": "causal MHA prefill B=4 Hq=Hkv=32 N=4096 d=128 + paged split-KV decode "
                                "B=8 Hq=32 Hkv=8 d=128 ctx U[1024,65536] seed 4, 16-token pages",
                    "parallelism": f"replicas x{world}", "num_splits": S,
-                   "l2": "flushed (256 MB write) before every timed launch"},
+                   "l2": "flushed before every timed launch: 256 MB written, then a separate 256 MB read"},
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak_t, "unit": "TFLOP/s",
                      "frac": tflops / peak_t, "traffic": recorded_traffic("prefill_tc_kernel<128>"),
                      "peak_source": f"{peak_src} bf16_tflops (burst)", "kernel": "prefill_tc_kernel<128>"},
@@ -389,6 +459,7 @@ def main():
                                 "frac": gbs / peak_b, "traffic": recorded_traffic("decode_kernel<128, page16>"),
                                 "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel<128, page16>"}},
         "prefill_ms": t_pre,
+        "block_sparse": sparse,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
