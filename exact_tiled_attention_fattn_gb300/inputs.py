@@ -178,22 +178,11 @@ def prefill_varlen(seed: int, lengths_range: tuple[int, int] | None, n_seqs: int
                          cu_seqlens=torch.tensor(cu, dtype=torch.int32), lengths=[int(n) for n in lengths])
 
 
-def decode_paged(seed: int, B: int, Hq: int, Hkv: int, d: int, page_size: int,
-                 context_range: tuple[int, int] | None, max_context: int,
-                 spare_pages: int = 0, dtype: torch.dtype = torch.bfloat16,
-                 scale: float | None = None, lengths: list[int] | None = None) -> DecodeInputs:
-    """Paged decode inputs: contexts uniform in ``context_range`` (inclusive).
-
-    The pool holds exactly the pages the sequences need plus ``spare_pages``;
-    pages are handed out through a random permutation of the pool, so logical
-    page p of sequence b lives at ``block_table[b, p]``.
-    """
-    g = torch.Generator("cpu").manual_seed(seed)
-    if lengths is None:
-        lo, hi = context_range
-        lengths = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
-    lengths = [int(n) for n in lengths]
-    assert len(lengths) == B and max(lengths) <= max_context
+def _page_pool(g: torch.Generator, lengths: list[int], page_size: int, max_context: int, spare_pages: int):
+    """Block table over a pool of exactly the pages ``lengths`` need plus ``spare_pages``,
+    handed out through a random permutation (one draw from ``g``). Table entries past a
+    sequence's pages point at spare pages (round robin) or at page 0 when there are none."""
+    B = len(lengths)
     pages = [(n + page_size - 1) // page_size for n in lengths]
     used = sum(pages)
     pool = used + spare_pages
@@ -212,22 +201,135 @@ def decode_paged(seed: int, B: int, Hq: int, Hkv: int, d: int, page_size: int,
             else:
                 table[b, pages[b]:] = 0
         off += pages[b]
-    q32 = _randn(g, (B, Hq, d))
-    k32 = _randn(g, (pool, page_size, Hkv, d))
-    v32 = _randn(g, (pool, page_size, Hkv, d))
-    # Slots that belong to no sequence: spare pages and the tail of each last page.
-    if spare_pages > 0:
+    return table, pages, pool, spare
+
+
+def _fill_unowned(k32, v32, table, pages, lengths, spare, page_size: int):
+    """Slots that belong to no sequence (spare pages, the tail of each last page) get SENTINEL."""
+    if len(spare) > 0:
         k32[spare] = SENTINEL
         v32[spare] = SENTINEL
-    for b in range(B):
-        tail = lengths[b] % page_size
+    for b, n in enumerate(lengths):
+        tail = n % page_size
         if tail:
             last = int(table[b, pages[b] - 1])
             k32[last, tail:] = SENTINEL
             v32[last, tail:] = SENTINEL
+
+
+def decode_paged(seed: int, B: int, Hq: int, Hkv: int, d: int, page_size: int,
+                 context_range: tuple[int, int] | None, max_context: int,
+                 spare_pages: int = 0, dtype: torch.dtype = torch.bfloat16,
+                 scale: float | None = None, lengths: list[int] | None = None) -> DecodeInputs:
+    """Paged decode inputs: contexts uniform in ``context_range`` (inclusive).
+
+    The pool holds exactly the pages the sequences need plus ``spare_pages``;
+    pages are handed out through a random permutation of the pool, so logical
+    page p of sequence b lives at ``block_table[b, p]``.
+    """
+    g = torch.Generator("cpu").manual_seed(seed)
+    if lengths is None:
+        lo, hi = context_range
+        lengths = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    lengths = [int(n) for n in lengths]
+    assert len(lengths) == B and max(lengths) <= max_context
+    table, pages, pool, spare = _page_pool(g, lengths, page_size, max_context, spare_pages)
+    q32 = _randn(g, (B, Hq, d))
+    k32 = _randn(g, (pool, page_size, Hkv, d))
+    v32 = _randn(g, (pool, page_size, Hkv, d))
+    _fill_unowned(k32, v32, table, pages, lengths, spare, page_size)
     s = 1.0 / math.sqrt(d) if scale is None else scale
     return DecodeInputs(q32, q32.to(dtype), k32.to(dtype), v32.to(dtype), table,
                         torch.tensor(lengths, dtype=torch.int32), page_size, s, spare_pages, lengths)
+
+
+@dataclass
+class PagedPrefillInputs:
+    """Multi-token queries against a paged KV cache (chunked prefill).
+
+    Sequence b owns context tokens [0, lengths_k[b]) in the cache; its
+    lengths_q[b] <= lengths_k[b] queries are the last lengths_q[b] of them,
+    packed back to back in q [Tq, Hq, d] with int32 cu_seqlens_q [B + 1].
+    kcache/vcache [num_pages, page_size, Hkv, d]; block_table int32
+    [B, max_pages_per_seq]; seqlens_k int32 [B]. Slots no sequence owns hold
+    ``SENTINEL``.
+    """
+
+    q32: torch.Tensor
+    q: torch.Tensor
+    kcache: torch.Tensor
+    vcache: torch.Tensor
+    block_table: torch.Tensor
+    seqlens_k: torch.Tensor
+    cu_seqlens_q: torch.Tensor
+    page_size: int
+    causal: bool
+    scale: float
+    lengths_q: list[int] = field(default_factory=list)
+    lengths_k: list[int] = field(default_factory=list)
+    spare_pages: int = 0
+
+    @property
+    def d(self) -> int:
+        return self.q.shape[-1]
+
+    @property
+    def hq(self) -> int:
+        return self.q.shape[1]
+
+    @property
+    def hkv(self) -> int:
+        return self.kcache.shape[2]
+
+    @property
+    def batch(self) -> int:
+        return len(self.lengths_q)
+
+    @property
+    def max_pages_per_seq(self) -> int:
+        return self.block_table.shape[1]
+
+    def flops(self) -> float:
+        """4*d FLOPs per (query, key) pair of each head: Lq*Lk pairs, or with the causal
+        rule Lq*(Lk - Lq) + Lq^2/2 (the dense convention for the square part)."""
+        pairs = 0.0
+        for lq, lk in zip(self.lengths_q, self.lengths_k):
+            pairs += lq * (lk - lq) + lq * lq / 2 if self.causal else lq * lk
+        return 4.0 * self.hq * self.d * pairs
+
+
+def prefill_paged(seed: int, B: int, Hq: int, Hkv: int, d: int, page_size: int,
+                  lengths_k: list[int] | tuple[int, int], lengths_q: list[int] | int | None,
+                  max_context: int, causal: bool = True, spare_pages: int = 0,
+                  dtype: torch.dtype = torch.bfloat16, scale: float | None = None) -> PagedPrefillInputs:
+    """Paged-prefill inputs. ``lengths_k``: a list, or a range (lo, hi) drawn uniform
+    inclusive; ``lengths_q``: a list, an int (chunk of min(int, Lk) queries per
+    sequence) or None (each drawn uniform in [1, Lk]). Draw order: context lengths,
+    query lengths, page permutation, Q, K, V."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    if isinstance(lengths_k, tuple):
+        lo, hi = lengths_k
+        lengths_k = torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+    lengths_k = [int(n) for n in lengths_k]
+    if lengths_q is None:
+        lengths_q = [int(torch.randint(1, n + 1, (1,), generator=g)) if n > 0 else 0 for n in lengths_k]
+    elif isinstance(lengths_q, int):
+        lengths_q = [min(lengths_q, n) for n in lengths_k]
+    lengths_q = [int(n) for n in lengths_q]
+    assert len(lengths_k) == len(lengths_q) == B and max(lengths_k) <= max_context
+    assert all(0 <= lq <= lk for lq, lk in zip(lengths_q, lengths_k))
+    table, pages, pool, spare = _page_pool(g, lengths_k, page_size, max_context, spare_pages)
+    cu = [0]
+    for n in lengths_q:
+        cu.append(cu[-1] + n)
+    q32 = _randn(g, (cu[-1], Hq, d))
+    k32 = _randn(g, (pool, page_size, Hkv, d))
+    v32 = _randn(g, (pool, page_size, Hkv, d))
+    _fill_unowned(k32, v32, table, pages, lengths_k, spare, page_size)
+    s = 1.0 / math.sqrt(d) if scale is None else scale
+    return PagedPrefillInputs(q32, q32.to(dtype), k32.to(dtype), v32.to(dtype), table,
+                              torch.tensor(lengths_k, dtype=torch.int32), torch.tensor(cu, dtype=torch.int32),
+                              page_size, causal, s, lengths_q, lengths_k, spare_pages)
 
 
 # ---- the five workloads (shapes of the pages' problems; sizes fixed here) ----

@@ -29,7 +29,7 @@ definition O = softmax(Q K^T * scale + M) V; the blocked modes restate the
 online-softmax rule and exist to pin the definition against the pages' worked
 example.
 
-Readings taken where the pages are silent (also listed in the design doc):
+Readings taken where the pages are silent:
   * statistics are exported as one natural-log logsumexp per row,
     lse = m + ln(l), over the scaled scores;
   * causal alignment is bottom-right: key j is allowed for query i when
@@ -60,6 +60,7 @@ __all__ = [
     "attention_blocked_normalised",
     "gather_paged",
     "decode_paged",
+    "attn_fwd_paged",
     "decode_split_ranges",
     "decode_partials",
     "merge_partials",
@@ -360,6 +361,49 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, scale: float):
         for h in range(Hq):
             ob, lb = attention_definition(q[b, h][None, :], kb[:, h // g], vb[:, h // g], scale, causal=True)
             o[b, h], lse[b, h] = ob[0], lb[0]
+    return o, lse
+
+
+def attn_fwd_paged(q, kcache, vcache, block_table, seqlens_k, cu_seqlens_q, scale: float, causal: bool,
+                   samples=None):
+    """Multi-token queries against a paged context (chunked prefill), by the definition.
+
+    Sequence b's queries q[cu[b]:cu[b+1]] (Lq of them) are the last Lq positions
+    of its Lk = seqlens_k[b] context tokens, read through the block table
+    ([FA-LLM] "Paged variants"; [CUDA-OPS] non-contiguous KV). With causal, query
+    i of the chunk sees keys j <= i + (Lk - Lq) (bottom-right alignment).
+    q [Tq, Hq, d] -> O [Tq, Hq, d], lse [Hq, Tq]; or, with samples (int
+    [n, 3] of (b, h, i)), O [n, d] and lse [n] at those rows only.
+    """
+    q = _f64(q)
+    cu = [int(x) for x in np.asarray(cu_seqlens_q)]
+    lens_k = [int(x) for x in np.asarray(seqlens_k)]
+    Tq, Hq, _ = q.shape
+    g = Hq // kcache.shape[2]
+    dv = vcache.shape[-1]
+    if samples is not None:
+        samples = np.asarray(samples, dtype=np.int64)
+        o = np.zeros((len(samples), dv))
+        lse = np.zeros(len(samples))
+        for b in sorted({int(x) for x in samples[:, 0]}):
+            kb = gather_paged(kcache, block_table, b, lens_k[b])
+            vb = gather_paged(vcache, block_table, b, lens_k[b])
+            qb = q[cu[b]:cu[b + 1]]
+            for n in np.nonzero(samples[:, 0] == b)[0]:
+                h, i = int(samples[n, 1]), int(samples[n, 2])
+                ob, lb = attention_definition(qb[:, h], kb[:, h // g], vb[:, h // g], scale, causal, rows=[i])
+                o[n], lse[n] = ob[0], lb[0]
+        return o, lse
+    o = np.zeros((Tq, Hq, dv))
+    lse = np.full((Hq, Tq), -np.inf)
+    for b in range(len(cu) - 1):
+        a, e = cu[b], cu[b + 1]
+        if e == a:
+            continue
+        kb = gather_paged(kcache, block_table, b, lens_k[b])
+        vb = gather_paged(vcache, block_table, b, lens_k[b])
+        for h in range(Hq):
+            o[a:e, h], lse[h, a:e] = attention_definition(q[a:e, h], kb[:, h // g], vb[:, h // g], scale, causal)
     return o, lse
 
 

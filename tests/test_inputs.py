@@ -46,3 +46,21 @@ def test_same_seed_same_bits():
 def test_flop_convention():
     x = inputs.prefill_dense(1, 4, 64, 2, 2, 16, causal=True)
     assert x.flops() == 4 * 4 * 2 * 64 * 64 * 16 / 2
+
+
+def test_paged_prefill_inputs():
+    x = inputs.prefill_paged(5, 3, 4, 2, 8, 16, (20, 100), None, 128, spare_pages=2)
+    assert len(x.lengths_k) == 3 and all(1 <= lq <= lk for lq, lk in zip(x.lengths_q, x.lengths_k))
+    cu = x.cu_seqlens_q.tolist()
+    assert cu[0] == 0 and cu[-1] == x.q.shape[0] == sum(x.lengths_q)
+    assert x.seqlens_k.tolist() == x.lengths_k
+    pages = [-(-n // 16) for n in x.lengths_k]
+    used = [p for b, n in enumerate(pages) for p in x.block_table[b, :n].tolist()]
+    assert len(set(used)) == len(used) == sum(pages) and x.kcache.shape[0] == sum(pages) + 2
+    for b, n in enumerate(x.lengths_k):
+        if n % 16:
+            last = int(x.block_table[b, pages[b] - 1])
+            assert torch.all(x.kcache[last, n % 16:].float() == inputs.SENTINEL)
+    y = inputs.prefill_paged(5, 2, 4, 2, 8, 16, [64, 30], 32, 64, causal=True)
+    assert y.lengths_q == [32, 30]
+    assert y.flops() == 4 * 4 * 8 * (32 * 32 + 32 * 32 / 2 + 30 * 30 / 2)

@@ -403,3 +403,62 @@ def test_block_sparse_all_ones_is_dense_and_empty_rows():
     for n, (b, h, i) in enumerate(smp):
         assert np.array_equal(os_[n], o[b, i, h]) or np.max(np.abs(os_[n] - o[b, i, h])) <= 1e-14
         assert (np.isneginf(ls_[n]) and np.isneginf(lse[b, h, i])) or abs(ls_[n] - lse[b, h, i]) <= 1e-14
+
+
+def test_paged_prefill_vs_python_loops():
+    """Chunked prefill over a paged context: query i of a chunk of Lq sees keys
+    j <= i + (Lk - Lq); the keys are gathered token by token through the table."""
+    rng = np.random.default_rng(30)
+    lens_k, lens_q = [5, 33, 17, 8], [5, 4, 1, 8]
+    Hq, Hkv, d, P = 4, 2, 3, 8
+    kc, vc, table, k_log, v_log = _small_paged(rng, lens_k, P, Hkv, d)
+    cu = np.concatenate([[0], np.cumsum(lens_q)])
+    q = _rand(rng, int(cu[-1]), Hq, d)
+    for causal in (False, True):
+        o, lse = orc.attn_fwd_paged(q, kc, vc, table, lens_k, cu, 0.4, causal)
+        for b, (lq, lk) in enumerate(zip(lens_q, lens_k)):
+            for h in range(Hq):
+                for i in range(lq):
+                    keys = [j for j in range(lk) if not causal or j <= i + lk - lq]
+                    krow = [kc[table[b, j // P], j % P, h // 2] for j in keys]
+                    vrow = [vc[table[b, j // P], j % P, h // 2] for j in keys]
+                    s = [0.4 * sum(float(q[cu[b] + i, h, c]) * float(kr[c]) for c in range(d)) for kr in krow]
+                    mx = max(s)
+                    w = [math.exp(x - mx) for x in s]
+                    tot = sum(w)
+                    ref = [sum(wi * float(vr[c]) for wi, vr in zip(w, vrow)) / tot for c in range(d)]
+                    assert np.max(np.abs(o[cu[b] + i, h] - np.array(ref))) <= 1e-13
+                    assert abs(lse[h, cu[b] + i] - (mx + math.log(tot))) <= 1e-13
+
+
+def test_paged_prefill_special_cases():
+    rng = np.random.default_rng(31)
+    lens_k = [9, 40, 16]
+    Hq, Hkv, d, P = 2, 1, 4, 16
+    kc, vc, table, k_log, v_log = _small_paged(rng, lens_k, P, Hkv, d)
+    # a full prefill from the cache (Lq = Lk): the first query sees key 0 only -> O = V[0]
+    cu = np.concatenate([[0], np.cumsum(lens_k)])
+    q = _rand(rng, int(cu[-1]), Hq, d)
+    o, lse = orc.attn_fwd_paged(q, kc, vc, table, lens_k, cu, 0.5, True)
+    for b in range(len(lens_k)):
+        for h in range(Hq):
+            assert np.max(np.abs(o[cu[b], h] - v_log[b][0, 0])) <= 1e-15
+    # chunks of one query are decode steps: the query sees its whole context
+    cu1 = np.arange(len(lens_k) + 1)
+    q1 = _rand(rng, len(lens_k), Hq, d)
+    o1, lse1 = orc.attn_fwd_paged(q1, kc, vc, table, lens_k, cu1, 0.5, True)
+    for b, n in enumerate(lens_k):
+        for h in range(Hq):
+            o_ref, l_ref = _python_attention([q1[b, h].tolist()], k_log[b][:, 0].tolist(),
+                                             v_log[b][:, 0].tolist(), 0.5, False)
+            assert np.max(np.abs(o1[b, h] - o_ref[0])) <= 1e-13 and abs(lse1[h, b] - l_ref[0]) <= 1e-13
+    # relabelling the pool's pages (and the table with them) changes nothing
+    perm = rng.permutation(kc.shape[0])
+    inv = np.argsort(perm)
+    o2, lse2 = orc.attn_fwd_paged(q, kc[perm], vc[perm], inv[table].astype(np.int32), lens_k, cu, 0.5, True)
+    assert np.array_equal(o2, o) and np.array_equal(lse2, lse)
+    # sampled rows agree with the full output
+    smp = np.array([[0, 1, 8], [1, 0, 0], [1, 1, 39], [2, 0, 7]])
+    os_, ls_ = orc.attn_fwd_paged(q, kc, vc, table, lens_k, cu, 0.5, True, samples=smp)
+    for n, (b, h, i) in enumerate(smp):
+        assert np.max(np.abs(os_[n] - o[cu[b] + i, h])) <= 1e-14 and abs(ls_[n] - lse[h, cu[b] + i]) <= 1e-14
