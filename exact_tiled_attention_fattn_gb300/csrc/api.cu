@@ -108,8 +108,7 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
   if (rows > 0x7fffffffLL || (long long)B * Hq * N > 0x7fffffffLL * 4LL) return FATTN_ERR_UNSUPPORTED;
 
   int err = 0;
-  PrefillParams p;
-  p.block_mask = nullptr;
+  PrefillParams p{};  // no block mask, no block table
   p.mask_heads = 1;
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = cu_seqlens;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
@@ -149,7 +148,7 @@ extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, con
   if (rows > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
 
   int err = 0;
-  PrefillParams p;
+  PrefillParams p{};
   p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
   p.causal = causal ? 1 : 0; p.scale = scale;
@@ -160,6 +159,48 @@ extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, con
   CUtensorMap tq, tk, tv;
   if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
       !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+    return FATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
+extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const void* vcache,
+                                        const int32_t* block_table, const int32_t* seqlens_k,
+                                        const int32_t* cu_seqlens_q, void* o, float* lse, int B, int Hq, int Hkv,
+                                        int d, int page_size, int max_pages_per_seq, int num_pages, int total_q,
+                                        int max_seqlen_q, int causal, float scale, cudaStream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || d <= 0 || total_q < 0 || max_seqlen_q < 0 || page_size <= 0 ||
+      max_pages_per_seq <= 0 || num_pages <= 0)
+    return FATTN_ERR_INVALID_ARG;
+  if (B == 0 || total_q == 0 || max_seqlen_q == 0) return FATTN_OK;
+  if (!q || !kcache || !vcache || !block_table || !seqlens_k || !cu_seqlens_q || !o) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kcache) || !aligned16(vcache) || !aligned16(o)) return FATTN_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(block_table) & 3u) || (reinterpret_cast<uintptr_t>(seqlens_k) & 3u) ||
+      (reinterpret_cast<uintptr_t>(cu_seqlens_q) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
+    return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  if (page_size != 16 && page_size != 32 && page_size != 64 && page_size != 128) return FATTN_ERR_UNSUPPORTED;
+  // pool rows, plus one box past the end for slots beyond a sequence's pages
+  if ((long long)(num_pages + 1) * page_size > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+  if ((long long)max_pages_per_seq * page_size > 0x7fffffffLL || (long long)B * max_pages_per_seq > 0x7fffffffLL)
+    return FATTN_ERR_UNSUPPORTED;
+
+  int err = 0;
+  PrefillParams p{};
+  p.q = q; p.k = kcache; p.v = vcache; p.o = o; p.lse = lse; p.cu_seqlens = cu_seqlens_q;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = max_seqlen_q; p.d = d; p.total_rows = total_q;
+  p.causal = causal ? 1 : 0; p.scale = scale;
+  p.mask_heads = 1;
+  p.block_table = block_table; p.seqlens_k = seqlens_k;
+  p.page_size = page_size; p.max_pages = max_pages_per_seq; p.num_pages = num_pages;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  const int pool_rows = num_pages * page_size;
+  if (!encode_rows_map(&tq, q, total_q, Hq, d, 128) || !encode_rows_map(&tk, kcache, pool_rows, Hkv, d, page_size) ||
+      !encode_rows_map(&tv, vcache, pool_rows, Hkv, d, page_size))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;

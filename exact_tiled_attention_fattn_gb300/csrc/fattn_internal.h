@@ -29,6 +29,11 @@ struct PrefillParams {
   // block (qb, kb) = 0 hides keys [128 kb, 128 kb + 128) from queries [128 qb, 128 qb + 128)
   const uint8_t* block_mask;  // nullptr = dense
   int mask_heads;             // 1 (shared by all heads) or Hq
+  // paged variant only (K/V read through a block table; q, o, lse packed as in
+  // varlen with cu_seqlens = the chunks' query offsets):
+  const int32_t* block_table; // device [B][max_pages]; nullptr = K/V in q's row space
+  const int32_t* seqlens_k;   // device [B]: context tokens per sequence (>= its queries)
+  int page_size, max_pages, num_pages;
 };
 
 // Longest mask row (blocks) the block-sparse kernel holds in shared memory.

@@ -117,7 +117,8 @@ enum : int {
 };
 
 struct Item {
-  int b, h, base, row0, L;
+  int b, h, base, row0, L;  // L: query rows of the sequence (its length, or the chunk's)
+  int Lk, off;              // keys of the sequence; query i sees keys j <= i + off if causal
   int n[2];   // K/V tiles tile A / tile B must visit (0: tile B has no row of the sequence)
   bool valid;
 };
@@ -166,24 +167,29 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, const Schedu
   if (p.cu_seqlens) {
     const int start = __ldg(p.cu_seqlens + x.b);
     const int end = __ldg(p.cu_seqlens + x.b + 1);
-    if (start < 0 || end < start || end > p.total_rows || end - start > p.N) {
+    // paged: the chunk's queries are the last L of the sequence's Lk context tokens
+    const int lk = p.seqlens_k ? __ldg(p.seqlens_k + x.b) : end - start;
+    if (start < 0 || end < start || end > p.total_rows || end - start > p.N ||
+        (p.seqlens_k && (lk < end - start || lk > p.max_pages * p.page_size))) {
       x.valid = false;
-      x.row0 = x.L = x.n[0] = x.n[1] = 0;
+      x.row0 = x.L = x.Lk = x.off = x.n[0] = x.n[1] = 0;
       if (pair == 0 && x.h == 0 && (threadIdx.x & 31) == 0) record_status(p.status, kStatusDeviceCheck);
       return x;
     }
     x.row0 = start;
     x.L = end - start;
+    x.Lk = lk;
   } else {
     x.row0 = x.b * p.N;
-    x.L = p.N;
+    x.L = x.Lk = p.N;
   }
+  x.off = x.Lk - x.L;
   x.valid = x.base < x.L;
-  const int kv_tiles = (x.L + BN - 1) / BN;
+  const int kv_tiles = (x.Lk + BN - 1) / BN;
   const bool has_b = x.base + BM < x.L;
-  if (p.causal) {
-    x.n[0] = min(x.base / BN + 1, kv_tiles);
-    x.n[1] = has_b ? min((x.base + BM) / BN + 1, kv_tiles) : 0;
+  if (p.causal) {  // up to the key the tile's last row sees
+    x.n[0] = min((min(x.base + BM, x.L) - 1 + x.off) / BN + 1, kv_tiles);
+    x.n[1] = has_b ? min((min(x.base + 2 * BM, x.L) - 1 + x.off) / BN + 1, kv_tiles) : 0;
   } else {
     x.n[0] = kv_tiles;
     x.n[1] = has_b ? kv_tiles : 0;
@@ -257,7 +263,7 @@ __device__ __forceinline__ float fmin3(float a, float b, float c) {
   return d;
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kPaged>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -332,14 +338,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sb + Lay::kOffQ + t * Lay::kQBytes + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h,
                         x.row0 + x.base + t * BM, pol_q);
         ++nq;
+        // K or V tile j (keys [128 j, 128 j + 128)) into one ring stage. Paged: one box
+        // of page_size rows per page, at the page's rows of the pool (read through the
+        // block table, each entry checked); slots past the sequence's last page read a
+        // box beyond the pool, which the copy fills with zeros. The boxes stack into the
+        // same swizzled layout as one 128-row box (page_size is a multiple of 8 rows).
+        auto issue_kv = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
+          if constexpr (kPaged) {
+            const int P = p.page_size, per = BN / P;
+            const int npages = (x.Lk + P - 1) / P;
+            const int32_t* bt = p.block_table + (size_t)x.b * p.max_pages;
+            for (int i = 0; i < per; ++i) {
+              const int slot = j * per + i;
+              int prow = p.num_pages * P;
+              if (slot < npages) {
+                const int pg = __ldg(bt + slot);
+                if (pg >= 0 && pg < p.num_pages)
+                  prow = pg * P;
+                else
+                  record_status(p.status, kStatusDeviceCheck);
+              }
+#pragma unroll
+              for (int dc = 0; dc < D / 64; ++dc)
+                tma_load_3d(dst + dc * BN * 128 + i * P * 128, map, full, dc * 64, hkv, prow, pol_kv);
+            }
+          } else {
+#pragma unroll
+            for (int dc = 0; dc < D / 64; ++dc)
+              tma_load_3d(dst + dc * BN * 128, map, full, dc * 64, hkv, x.row0 + j * BN, pol_kv);
+          }
+        };
         auto load_k = [&](int j) -> bool {
           const uint32_t st = nk & 1;
           if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
           mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
-#pragma unroll
-          for (int dc = 0; dc < D / 64; ++dc)
-            tma_load_3d(sb + Lay::kOffK + st * Lay::kKVBytes + dc * BN * 128, &tk, bar(kBarKFull + st), dc * 64,
-                        hkv, x.row0 + j * BN, pol_kv);
+          issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j);
           ++nk;
           return true;
         };
@@ -347,10 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = nv & 1;
           if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
           mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
-#pragma unroll
-          for (int dc = 0; dc < D / 64; ++dc)
-            tma_load_3d(sb + Lay::kOffV + st * Lay::kKVBytes + dc * BN * 128, &tv, bar(kBarVFull + st), dc * 64,
-                        hkv, x.row0 + j * BN, pol_kv);
+          issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j);
           ++nv;
           return true;
         };
@@ -648,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int row = x.base + t * BM + r;
-      const int lim = p.causal ? min(row + 1, x.L) : x.L;  // keys < lim are visible
+      const int lim = p.causal ? min(row + x.off + 1, x.Lk) : x.Lk;  // keys < lim are visible
       if constexpr (kSparse) {  // a tile that keeps no block: O = 0, lse = -inf
         if (kept_blocks == 0) {
           release_mask();
@@ -799,11 +829,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kSparse>
+template <int D, bool kSparse, bool kPaged>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      int num_sms, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<D, kSparse>;
+  auto kern = prefill_tc_kernel<D, kSparse, kPaged>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   const long long pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
@@ -819,11 +849,15 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
   if (p.block_mask) {
-    if (p.d == 128) return launch_t<128, true>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, true>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, true, false>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, true, false>(p, tq, tk, tv, num_sms, stream);
   }
-  if (p.d == 128) return launch_t<128, false>(p, tq, tk, tv, num_sms, stream);
-  return launch_t<64, false>(p, tq, tk, tv, num_sms, stream);
+  if (p.block_table) {
+    if (p.d == 128) return launch_t<128, false, true>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, false, true>(p, tq, tk, tv, num_sms, stream);
+  }
+  if (p.d == 128) return launch_t<128, false, false>(p, tq, tk, tv, num_sms, stream);
+  return launch_t<64, false, false>(p, tq, tk, tv, num_sms, stream);
 }
 
 }  // namespace fattn

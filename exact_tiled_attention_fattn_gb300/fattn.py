@@ -32,6 +32,8 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "fattn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _i, _vp]),
     "fattn_fwd_block_sparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
+    "fattn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
+                             _vp]),
     "fattn_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fattn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz,
                                 _vp]),
@@ -198,6 +200,44 @@ def fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | N
                                     1 if causal else 0, float(scale), _ptr(block_mask), block_mask.shape[0],
                                     ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_fwd_block_sparse", st)
+    return out, lse
+
+
+def fwd_paged(q, kcache, vcache, block_table, seqlens_k, cu_seqlens_q, max_seqlen_q: int, causal: bool = True,
+              scale: float | None = None, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Prefill of query chunks against a paged KV cache. q [Tq,Hq,d] bf16 packed by
+    int32 ``cu_seqlens_q`` [B+1]; chunk b holds the last Lq_b positions of sequence b's
+    ``seqlens_k[b]`` context tokens; kcache/vcache [pages, page_size, Hkv, d] bf16;
+    block_table int32 [B, max_pages_per_seq]. Returns (O [Tq,Hq,d], lse [Hq,Tq])."""
+    lib = load_library()
+    _need_cuda(q, kcache, vcache, block_table, seqlens_k, cu_seqlens_q, out, lse)
+    if not (q.dtype == kcache.dtype == vcache.dtype == torch.bfloat16):
+        raise TypeError("paged prefill takes bf16 q and caches")
+    if block_table.dtype != torch.int32 or seqlens_k.dtype != torch.int32 or cu_seqlens_q.dtype != torch.int32:
+        raise TypeError("block_table, seqlens_k and cu_seqlens_q must be int32")
+    if q.dim() != 3 or kcache.dim() != 4:
+        raise ValueError("q must be [Tq, Hq, d] and kcache [pages, page_size, Hkv, d]")
+    Tq, Hq, d = q.shape
+    num_pages, page_size, Hkv, _ = kcache.shape
+    B = cu_seqlens_q.numel() - 1
+    _expect(kcache, (num_pages, page_size, Hkv, d), "kcache")
+    _expect(vcache, kcache.shape, "vcache")
+    if block_table.dim() != 2 or block_table.shape[0] != B:
+        raise ValueError(f"block_table must be [{B}, max_pages_per_seq]")
+    _expect(seqlens_k, (B,), "seqlens_k")
+    _expect(out, q.shape, "out", q.dtype)
+    _expect(lse, (Hq, Tq), "lse", torch.float32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((Hq, Tq), dtype=torch.float32, device=q.device)
+    st = lib.fattn_fwd_paged(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(block_table), _ptr(seqlens_k),
+                             _ptr(cu_seqlens_q), _ptr(out), _ptr(lse), B, Hq, Hkv, d, page_size,
+                             block_table.shape[1], num_pages, Tq, int(max_seqlen_q), 1 if causal else 0,
+                             float(scale), ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_fwd_paged", st)
     return out, lse
 
 

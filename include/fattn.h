@@ -111,6 +111,40 @@ fattn_status fattn_fwd_block_sparse(const void* q, const void* k, const void* v,
                                     const uint8_t* block_mask, int mask_heads, cudaStream_t stream);
 
 /*
+ * fattn_fwd_paged — prefill of query chunks against a paged KV cache
+ * (chunked prefill, or a whole prompt read back from the cache).
+ * [FA-LLM] "Paged variants" (the tiled computation with K/V read through a
+ * block table); [FA-PAPER] "The forward pass" (the computation itself).
+ *
+ * q [total_q, Hq, d] bf16: B chunks packed back to back; chunk b is rows
+ *   [cu_seqlens_q[b], cu_seqlens_q[b+1]) (Lq_b rows) and holds the queries of
+ *   the LAST Lq_b positions of sequence b's context.
+ * kcache, vcache [num_pages, page_size, Hkv, d] bf16: token t of sequence b is
+ *   slot t % page_size of page block_table[b * max_pages_per_seq + t / page_size].
+ * seqlens_k [B] int32, cu_seqlens_q [B + 1] int32, block_table int32: DEVICE.
+ *   seqlens_k[b] counts the context tokens including the chunk's own:
+ *   Lq_b <= seqlens_k[b] <= max_pages_per_seq * page_size.
+ * o [total_q, Hq, d] bf16; lse [Hq, total_q] fp32 (may be NULL).
+ * causal != 0: query i of chunk b sees keys j <= i + seqlens_k[b] - Lq_b.
+ * max_seqlen_q: host upper bound on every Lq_b (sizes the grid).
+ * Supported: d in {64, 128}, page_size in {16, 32, 64, 128}.
+ * Slots past seqlens_k[b] in a sequence's last page are read and get weight 0,
+ *   so they must hold finite values; table entries past the last page are not read.
+ * Errors: INVALID_ARG (NULL or misaligned pointers, negative sizes,
+ *   Hq % Hkv != 0, non-finite scale); UNSUPPORTED (d, page_size,
+ *   (num_pages + 1) * page_size >= 2^31). A table entry outside
+ *   [0, num_pages) (read as zeros), a seqlens_k outside the range above or a
+ *   bad cu_seqlens_q (chunk skipped) record FATTN_ERR_DEVICE_CHECK in the
+ *   status word.
+ */
+fattn_status fattn_fwd_paged(const void* q, const void* kcache, const void* vcache,
+                             const int32_t* block_table, const int32_t* seqlens_k,
+                             const int32_t* cu_seqlens_q, void* o, float* lse,
+                             int B, int Hq, int Hkv, int d, int page_size, int max_pages_per_seq,
+                             int num_pages, int total_q, int max_seqlen_q, int causal, float scale,
+                             cudaStream_t stream);
+
+/*
  * fattn_decode_workspace_size — bytes of scratch fattn_decode_paged needs:
  * the per-split partials lse_part [B, Hq, S] fp32 and o_part [B, Hq, S, d]
  * fp32 (S = num_splits), then 1 + B * Hq int32 work-scheduling counters, each

@@ -32,7 +32,8 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted(fattn.SIGNATURES), "binding signatures must mirror include/fattn.h"
     for n in names:
         assert hasattr(lib, n), n
-    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_decode_workspace_size", "fattn_decode_paged",
+    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_paged", "fattn_decode_workspace_size",
+                          "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
                           "fattn_debug_read_status"}
 
@@ -135,3 +136,21 @@ def test_block_sparse_validation(lib):
     assert f(d=80) == E.FATTN_ERR_UNSUPPORTED
     assert f(N=2048 * 128 + 1) == E.FATTN_ERR_UNSUPPORTED  # mask rows longer than 2048 blocks
     assert f(B=0, q=None, m=None) == E.FATTN_OK          # empty problem
+
+
+def test_paged_prefill_validation(lib):
+    E = fattn
+
+    def f(**kw):
+        g = lambda n, dflt: kw.get(n, dflt)
+        return lib.fattn_fwd_paged(g("q", A), g("kc", A), A, g("bt", A), A, A, A, None, g("B", 2), g("Hq", 4),
+                                   g("Hkv", 2), g("d", 128), g("P", 16), g("maxp", 8), g("pages", 64),
+                                   g("Tq", 100), g("maxq", 64), 1, 0.1, None)
+    assert f(bt=None) == E.FATTN_ERR_INVALID_ARG
+    assert f(kc=A + 4) == E.FATTN_ERR_INVALID_ARG
+    assert f(Hkv=3) == E.FATTN_ERR_INVALID_ARG
+    assert f(pages=0) == E.FATTN_ERR_INVALID_ARG
+    assert f(d=96) == E.FATTN_ERR_UNSUPPORTED
+    assert f(P=8) == E.FATTN_ERR_UNSUPPORTED and f(P=48) == E.FATTN_ERR_UNSUPPORTED
+    assert f(pages=(1 << 31) // 16) == E.FATTN_ERR_UNSUPPORTED    # pool rows past int32
+    assert f(Tq=0, q=None, bt=None) == E.FATTN_OK                  # empty problem
