@@ -308,7 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsControlSparse : kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // Lane 0 issues every copy; the paged variant runs lanes 0-7 through the same
+    // loop (each lane waits on the same barriers) and lane i copies page i of a tile,
+    // because one thread issuing a tile's 2 x (128 / page_size) boxes in sequence
+    // cannot keep up with the tensor core for small pages.
+    const bool leader = lane == 0;
+    if (kPaged ? lane < BN / 16 : leader) {
       uint32_t nq = 0, nk = 0, nv = 0, nm = 0;
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
       for (int k = 0;; ++k) {
@@ -330,13 +335,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (!mbar_wait(bar(kBarQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
-        mbar_arrive_expect_tx(bar(kBarQFull), 2 * Lay::kQBytes);
+        if (leader) {
+          mbar_arrive_expect_tx(bar(kBarQFull), 2 * Lay::kQBytes);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+          for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int dc = 0; dc < D / 64; ++dc)
-            tma_load_3d(sb + Lay::kOffQ + t * Lay::kQBytes + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h,
-                        x.row0 + x.base + t * BM, pol_q);
+            for (int dc = 0; dc < D / 64; ++dc)
+              tma_load_3d(sb + Lay::kOffQ + t * Lay::kQBytes + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h,
+                          x.row0 + x.base + t * BM, pol_q);
+        }
         ++nq;
         // K or V tile j (keys [128 j, 128 j + 128)) into one ring stage. Paged: one box
         // of page_size rows per page, at the page's rows of the pool (read through the
@@ -345,14 +352,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // same swizzled layout as one 128-row box (page_size is a multiple of 8 rows).
         auto issue_kv = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
           if constexpr (kPaged) {
-            const int P = p.page_size, per = BN / P;
-            const int npages = (x.Lk + P - 1) / P;
-            const int32_t* bt = p.block_table + (size_t)x.b * p.max_pages;
-            for (int i = 0; i < per; ++i) {
+            const int P = p.page_size, per = BN / P;  // per <= 8 (page_size >= 16)
+            const int i = lane;                       // this lane's page of the tile
+            if (i < per) {
               const int slot = j * per + i;
               int prow = p.num_pages * P;
-              if (slot < npages) {
-                const int pg = __ldg(bt + slot);
+              if (slot < (x.Lk + P - 1) / P) {
+                const int pg = __ldg(p.block_table + (size_t)x.b * p.max_pages + slot);
                 if (pg >= 0 && pg < p.num_pages)
                   prow = pg * P;
                 else
@@ -371,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_k = [&](int j) -> bool {
           const uint32_t st = nk & 1;
           if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
-          mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
+          // a lane's copy may complete before the leader's expect: the phase still needs the leader's arrival
+          if (leader) mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
           issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j);
           ++nk;
           return true;
@@ -379,7 +386,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto load_v = [&](int j) -> bool {
           const uint32_t st = nv & 1;
           if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
-          mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
+          if (leader) mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
           issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j);
           ++nv;
           return true;
