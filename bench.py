@@ -45,11 +45,12 @@ def parse():
     ap.add_argument("--num-splits", type=int, default=0, help="decode splits (0 = library heuristic)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-sparse", action="store_true", help="skip the block-sparse prefill measurement")
+    ap.add_argument("--no-sparse", action="store_true",
+                    help="skip the block-sparse and paged prefill measurements (outside the step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--profile-once", action="store_true",
-                    help="one prefill, one decode and one block-sparse launch on the bench workloads, "
-                         "then exit (for ncu)")
+                    help="one launch each of prefill, decode, block-sparse and paged prefill on the bench "
+                         "workloads, then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -58,6 +59,7 @@ KERNEL_SOURCES = {
     "decode_kernel<128, page16>": ["decode.cu", "device_common.cuh", "fattn_internal.h"],
 }
 KERNEL_SOURCES["prefill_tc_kernel<128, sparse>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["prefill_tc_kernel<128, paged>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 
 
 def recorded_traffic(kernel: str):
@@ -207,6 +209,42 @@ def block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks):
     return res
 
 
+def paged_prefill_workload():
+    """Chunked prefill: B=4, Hq=32, Hkv=8, d=128, 16-token pages, contexts U[4096, 16384]
+    (seed 710), the last 2048 positions of each context as the chunk's queries."""
+    from exact_tiled_attention_fattn_gb300 import inputs
+    return inputs.prefill_paged(710, 4, 32, 8, 128, 16, (4096, 16384), 2048, 16384, causal=True)
+
+
+def paged_prefill_leg(fattn, flush, stream, peaks, dev):
+    """fattn_fwd_paged on the chunked-prefill workload (10 launches, median)."""
+    import torch
+    x = paged_prefill_workload()
+    args = [t.to(dev) for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q)]
+    o = torch.empty_like(args[0])
+    lse = torch.empty((x.hq, args[0].shape[0]), dtype=torch.float32, device=dev)
+    run = lambda: fattn.fwd_paged(*args, max(x.lengths_q), causal=True, scale=x.scale, out=o, lse=lse)
+    for _ in range(3):
+        flush()
+        run()
+    ts = []
+    for _ in range(10):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    t = statistics.median(ts)
+    tf = x.flops() / (t * 1e-3) / 1e12
+    kv = 2 * sum(x.lengths_k) * x.hkv * x.d * 2
+    return {"workload": "chunked prefill B=4 Hq=32 Hkv=8 d=128, 16-token pages, contexts U[4096,16384] seed 710 "
+                        f"({sum(x.lengths_k)} tokens), 2048-query chunks, causal bottom-right",
+            "ms": t, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"], "flops": x.flops(),
+            "kv_bytes": kv, "traffic": recorded_traffic("prefill_tc_kernel<128, paged>")}
+
+
 def cpu_baseline_prefill(pre, seconds: float):
     """Time the fp64 oracle on sampled query rows of the prefill workload."""
     import numpy as np
@@ -310,6 +348,9 @@ def main():
             nb = pre.q.shape[1] // 128
             mt = torch.from_numpy(local_global_mask(nb, 3)).to(dev)
             fattn.fwd_block_sparse(q, k, v, mt, causal=True, scale=pre.scale, out=o, lse=lse)
+            x = paged_prefill_workload()            # and one paged (chunked) prefill launch
+            pa = [t.to(dev) for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q)]
+            fattn.fwd_paged(*pa, max(x.lengths_q), causal=True, scale=x.scale)
         torch.cuda.synchronize()
         st = fattn.debug_read_status()
         print(json.dumps({"profile_once": True, "num_splits": S, "device_status": st}), flush=True)
@@ -423,6 +464,7 @@ def main():
                "decode": {"value": world * kv_bytes / (td * 1e-3) / 1e9, "unit": "GB/s"}}
 
     sparse = None if args.no_sparse else block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks)
+    paged = None if args.no_sparse else paged_prefill_leg(fattn, flush, stream, peaks, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -460,6 +502,7 @@ def main():
                                 "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel<128, page16>"}},
         "prefill_ms": t_pre,
         "block_sparse": sparse,
+        "paged_prefill": paged,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
