@@ -19,6 +19,9 @@ Sources (three web pages on one subject):
             statistics l and m).
   [CUDA-OPS] "Attention" CUDA operations guide (rightnowai.co): K/V heads shared
             by several Q heads (GQA/MQA); non-contiguous (paged) KV allocation.
+  [FA-PAPER] "The backward pass recomputes instead of reading": P rebuilt from
+            the saved statistics; dV += P^T dO, dP = dO V^T,
+            dS = P o (dP - D) with D = rowsum(dO o O), dQ += dS K, dK += dS^T Q.
   [FA-PAPER] "Block-sparse FlashAttention": a fixed mask over blocks; every
             block that is zero in the mask is skipped, i.e. its scores are
             excluded from the softmax (an approximation of dense attention).
@@ -37,6 +40,9 @@ Readings taken where the pages are silent:
   * query head h reads KV head h // (Hq / Hkv);
   * a row with no allowed key has O = 0 and lse = -inf; a partial with
     lse = -inf carries no weight in a merge;
+  * backward: the page writes the gradient steps for S = Q K^T; with the
+    scale, S = scale * Q K^T, so dQ = scale * dS K and dK = scale * dS^T Q
+    (chain rule); GQA: a KV head's dK, dV sum over the query heads sharing it;
   * decode splits: with P_b = ceil(L_b / page_size) pages and
     C = ceil(max_pages_per_seq / num_splits) pages per split, split s of
     sequence b covers tokens [s*C*page_size, min(L_b, (s+1)*C*page_size)),
@@ -61,6 +67,7 @@ __all__ = [
     "gather_paged",
     "decode_paged",
     "attn_fwd_paged",
+    "attn_bwd",
     "decode_split_ranges",
     "decode_partials",
     "merge_partials",
@@ -405,6 +412,39 @@ def attn_fwd_paged(q, kcache, vcache, block_table, seqlens_k, cu_seqlens_q, scal
         for h in range(Hq):
             o[a:e, h], lse[h, a:e] = attention_definition(q[a:e, h], kb[:, h // g], vb[:, h // g], scale, causal)
     return o, lse
+
+
+def attn_bwd(q, k, v, do, scale: float, causal: bool):
+    """Gradients of L = sum(O o dO) for dense q [B, N, Hq, d], k/v [B, N, Hkv, d], fp64.
+
+    Per (b, h), with whole matrices as the one block ([FA-PAPER] "The backward
+    pass recomputes instead of reading"): P = softmax(scale Q K^T + M),
+    O = P V, D = rowsum(dO o O), dV = P^T dO, dP = dO V^T, dS = P o (dP - D),
+    dQ = scale dS K, dK = scale dS^T Q. Returns (dq, dk, dv) in the input layouts.
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    do = _f64(do)
+    B, N, Hq, _ = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(Hq):
+            kh, vh = k[b, :, h // g], v[b, :, h // g]
+            p = attention_weights(q[b, :, h], kh, scale, causal)      # [N, N]
+            o = p @ vh
+            dOh = do[b, :, h]
+            dmat = np.sum(dOh * o, axis=1)                           # D = rowsum(dO o O)
+            dv[b, :, h // g] += p.T @ dOh                            # dV = P^T dO
+            dp = dOh @ vh.T                                          # dP = dO V^T
+            ds = p * (dp - dmat[:, None])                            # dS = P o (dP - D)
+            dq[b, :, h] = scale * (ds @ kh)                          # dQ = scale dS K
+            dk[b, :, h // g] += scale * (ds.T @ q[b, :, h])          # dK = scale dS^T Q
+    return dq, dk, dv
 
 
 def decode_split_ranges(seqlens, page_size: int, max_pages_per_seq: int, num_splits: int):

@@ -462,3 +462,68 @@ def test_paged_prefill_special_cases():
     os_, ls_ = orc.attn_fwd_paged(q, kc, vc, table, lens_k, cu, 0.5, True, samples=smp)
     for n, (b, h, i) in enumerate(smp):
         assert np.max(np.abs(os_[n] - o[cu[b] + i, h])) <= 1e-14 and abs(ls_[n] - lse[h, cu[b] + i]) <= 1e-14
+
+
+def _loss(q, k, v, do, scale, causal):
+    o, _ = orc.attn_fwd(q, k, v, scale, causal)
+    return float(np.sum(o * do))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_matches_finite_differences(causal):
+    """dQ, dK, dV are the gradients of L = sum(O o dO): central differences on every input."""
+    rng = np.random.default_rng(40)
+    B, N, Hq, Hkv, d, sc = 1, 5, 2, 1, 3, 0.7
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    do = _rand(rng, B, N, Hq, d)
+    dq, dk, dv = orc.attn_bwd(q, k, v, do, sc, causal)
+    eps = 1e-6
+    for x, gx in ((q, dq), (k, dk), (v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + eps
+            lp = _loss(q, k, v, do, sc, causal)
+            x[idx] = old - eps
+            lm = _loss(q, k, v, do, sc, causal)
+            x[idx] = old
+            num[idx] = (lp - lm) / (2 * eps)
+        assert np.max(np.abs(num - gx)) <= 1e-7
+
+
+def test_backward_matches_torch_autograd():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(41)
+    B, N, Hq, Hkv, d, sc = 2, 9, 4, 2, 6, 0.4
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    do = _rand(rng, B, N, Hq, d)
+    for causal in (False, True):
+        tq, tk, tv = (torch.tensor(a, dtype=torch.float64, requires_grad=True) for a in (q, k, v))
+        kk = tk.repeat_interleave(Hq // Hkv, dim=2)
+        vv = tv.repeat_interleave(Hq // Hkv, dim=2)
+        s = sc * torch.einsum("bihc,bjhc->bhij", tq, kk)
+        if causal:
+            s = s.masked_fill(torch.ones(N, N, dtype=torch.bool).triu(1), float("-inf"))
+        o = torch.einsum("bhij,bjhc->bihc", torch.softmax(s, dim=-1), vv)
+        (o * torch.tensor(do)).sum().backward()
+        dq, dk, dv = orc.attn_bwd(q, k, v, do, sc, causal)
+        for mine, ref in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+            assert np.max(np.abs(mine - ref.numpy())) <= 1e-12
+
+
+def test_backward_closed_form_uniform_causal():
+    """K = 0: row i of P is uniform over keys 0..i, so dV_j = sum_{i >= j} dO_i / (i + 1);
+    and with every row's dO equal to c, O's gradient through V is all there is: dQ = dK = 0
+    when V is constant along keys."""
+    rng = np.random.default_rng(42)
+    B, N, H, d = 1, 6, 1, 3
+    q, v, do = _rand(rng, B, N, H, d), _rand(rng, B, N, H, d), _rand(rng, B, N, H, d)
+    k = np.zeros((B, N, H, d))
+    _, _, dv = orc.attn_bwd(q, k, v, do, 0.5, True)
+    for j in range(N):
+        ref = sum(do[0, i, 0] / (i + 1) for i in range(j, N))
+        assert np.max(np.abs(dv[0, j, 0] - ref)) <= 1e-14
+    vc = np.repeat(_rand(rng, 1, 1, 1, d), N, axis=1)
+    kr = _rand(rng, B, N, H, d)
+    dq, dk, _ = orc.attn_bwd(q, kr, vc, do, 0.5, False)
+    assert np.max(np.abs(dq)) <= 1e-13 and np.max(np.abs(dk)) <= 1e-13
