@@ -209,6 +209,50 @@ extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+extern "C" size_t fattn_bwd_workspace_size(int B, int Hq, int N) {
+  if (B <= 0 || Hq <= 0 || N <= 0) return 0;
+  const size_t npad = ((size_t)N + 127) / 128 * 128;
+  return 2 * align256((size_t)B * Hq * npad * sizeof(float));
+}
+
+extern "C" fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                                  int d, int causal, float scale, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * N;
+  const long long npad = ((long long)N + 127) / 128 * 128;
+  if (rows > 0x7fffffffLL || (long long)B * Hq * npad > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+  const size_t need = fattn_bwd_workspace_size(B, Hq, N);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FATTN_ERR_WORKSPACE;
+
+  int err = 0;
+  BwdParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  p.ws_lse2 = static_cast<float*>(workspace);
+  p.ws_d = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Npad = (int)npad;
+  p.causal = causal ? 1 : 0; p.scale = scale;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!encode_rows_map(&tq, q, (int)rows, Hq, d, 128) || !encode_rows_map(&tk, k, (int)rows, Hkv, d, 128) ||
+      !encode_rows_map(&tv, v, (int)rows, Hkv, d, 128) || !encode_rows_map(&tdo, dout, (int)rows, Hq, d, 128))
+    return FATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return FATTN_ERR_CUDA;
+  return launch_backward(p, tq, tk, tv, tdo, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 extern "C" size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits) {
   if (B <= 0 || Hq <= 0 || d <= 0 || num_splits <= 0) return 0;
   size_t rows = (size_t)B * Hq * num_splits;

@@ -1,0 +1,697 @@
+// Tensor-core attention backward for sm_103a ("The backward pass recomputes
+// instead of reading", FlashAttention explained): P is rebuilt tile by tile
+// from the saved logsumexp, never read from HBM, and
+//   D = rowsum(dO o O),  dV += P^T dO,  dP = dO V^T,  dS = P o (dP - D),
+//   dQ += scale dS K,    dK += scale dS^T Q     (S = scale Q K^T).
+//
+// Three launches on the caller's stream:
+//   bwd_preprocess_kernel  D and lse * log2(e) per query row, into a workspace
+//                          padded to whole 128-row tiles (pad: D = 0,
+//                          lse = +inf, so padded rows get P = 0).
+//   bwd_dkdv_kernel<d>     one CTA per SM over items (sequence, KV head, 128-key
+//                          tile j); an item walks the query tiles i of every
+//                          query head sharing the KV head (causal: i >= j) and
+//                          accumulates dV and dK in TMEM:
+//                            S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, fp32),
+//                            P^T (bf16, over S^T), dV += P^T dO_i,
+//                            dS^T (bf16, over dP^T), dK += dS^T Q_i.
+//   bwd_dq_kernel<d>       items (sequence, query head, 128-query tile i); an
+//                          item walks the key tiles j (causal: j <= i):
+//                            S = Q K_j^T, dP = dO V_j^T, dS (bf16, over dP),
+//                            dQ += dS K_j.
+// dQ is computed in its own pass (recomputing S and dP) instead of being
+// accumulated with atomics from the dK/dV pass: at d = 128 the dK/dV pass
+// already uses all 512 TMEM columns (S^T, dP^T, dV, dK).
+//
+// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread),
+// warps 4-7 the element-wise work, one thread per TMEM lane (tile row).
+// Every pipeline wait is bounded as in the forward kernel: a wait past its
+// limit records FATTN_ERR_TIMEOUT, every role stops, copies and MMAs are
+// drained and TMEM is freed.
+#include "device_common.cuh"
+#include "fattn_internal.h"
+#include "sm100_primitives.cuh"
+
+#include <math_constants.h>
+
+#include <algorithm>
+
+namespace fattn {
+namespace {
+
+using namespace sm100;
+
+constexpr int BT = 128;          // rows of every tile (query rows or keys)
+constexpr int kThreads = 256;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+// TMEM columns (both passes): S or S^T at 0 (P / P^T in bf16 over its first 64
+// columns), dP or dP^T at 128 (dS in bf16 over its first 64), accumulators at 256.
+constexpr uint32_t kColS = 0, kColDP = 128, kColAcc = 256;
+
+__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > kDrainLimitNs) break;
+  }
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// ------------------------------------------------------------------ preprocess
+// One warp per row of the padded [B * Hq, Npad] workspace.
+__global__ void bwd_preprocess_kernel(const BwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const long long rows = (long long)p.B * p.Hq * p.Npad;
+  const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
+    const int bh = (int)(r / p.Npad), i = (int)(r - (long long)bh * p.Npad);
+    float dsum = 0.f, l2 = CUDART_INF_F;
+    if (i < p.N) {
+      const int b = bh / p.Hq, h = bh - b * p.Hq;
+      const size_t off = (((size_t)b * p.N + i) * p.Hq + h) * p.d;
+      const uint32_t* o2 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.o) + off);
+      const uint32_t* g2 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.dout) + off);
+      for (int c = lane; c < p.d / 2; c += 32) {
+        const uint32_t a = __ldg(o2 + c), g = __ldg(g2 + c);
+        dsum = fmaf(bf16_lo(a), bf16_lo(g), dsum);
+        dsum = fmaf(bf16_hi(a), bf16_hi(g), dsum);
+      }
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
+      const float lse = __ldg(p.lse + (size_t)bh * p.N + i);
+      if (lse > -CUDART_INF_F && lse < CUDART_INF_F) l2 = lse * kLog2e;  // a row with no key: P = 0
+    }
+    if (lane == 0) {
+      p.ws_lse2[r] = l2;
+      p.ws_d[r] = dsum;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ shared helpers
+template <int D>
+struct BwdTiles {
+  static constexpr int kTile = BT * D * 2;   // one 128-row bf16 tile (D / 64 swizzled 64-column halves)
+  static constexpr int kAtom = BT * 128 / 16;  // 16-byte units between the 64-column halves
+};
+
+// K-major x K-major product D[tmem] = A B^T over the head dimension (128 x 128 x D).
+template <int D>
+__device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint64_t a0, uint64_t b0) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, BT, 0);
+  mma_ss_c<false>(d_tmem, a0, b0, id);
+#pragma unroll
+  for (int ks = 1; ks < D / 16; ++ks) {
+    const uint64_t o = (uint64_t)((ks >> 2) * BwdTiles<D>::kAtom + (ks & 3) * 2);
+    mma_ss_c<true>(d_tmem, a0 + o, b0 + o, id);
+  }
+}
+// D[tmem] (+)= A[tmem] B over 128 rows of B (B MN-major: the head dimension contiguous).
+template <int D>
+__device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, bool acc) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, D, 1);
+  mma_ts(d_tmem, a_tmem, b0, id, acc ? 1u : 0u);
+#pragma unroll
+  for (int ks = 1; ks < BT / 16; ++ks) mma_ts_acc(d_tmem, a_tmem + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), id);
+}
+
+// Load 128-row tile (rows r0.., head h) of a [rows, H, D] tensor map into dst.
+template <int D>
+__device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int h, int r0,
+                                          uint64_t pol) {
+#pragma unroll
+  for (int dc = 0; dc < D / 64; ++dc) tma_load_3d(dst + dc * BT * 128, map, bar, dc * 64, h, r0, pol);
+}
+
+// Write one accumulator row (D fp32 TMEM columns) times `mul` as bf16.
+template <int D>
+__device__ __forceinline__ void store_row(uint32_t t_col, float mul, __nv_bfloat16* dst, bool live) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t u[32];
+    tmem_ld32(t_col + 32 * c, u);
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
+    if (live) {
+      uint4* q = reinterpret_cast<uint4*>(dst + 32 * c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) q[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+  }
+}
+
+// dS = P o (dP - Dvec) for the 128 columns of this lane, written as bf16 over
+// the first 64 columns of the dP buffer, 32 columns at a time: pass q reads dP
+// columns [32q, 32q + 32) and then writes packed columns [16q, 16q + 16), all of
+// which the same or an earlier pass has already read.
+template <typename DAt>
+__device__ __forceinline__ void write_ds(uint32_t dp_col, const float (&pv)[BT], DAt dvec) {
+#pragma unroll
+  for (int q = 0; q < BT / 32; ++q) {
+    uint32_t a[32];
+    tmem_ld32(dp_col + 32 * q, a);
+    uint32_t w[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int c = 32 * q + 2 * e;
+      w[e] = pack_bf16x2(pv[c] * (__uint_as_float(a[2 * e]) - dvec(c)),
+                         pv[c + 1] * (__uint_as_float(a[2 * e + 1]) - dvec(c + 1)));
+    }
+    tmem_st16(dp_col + 16 * q, w);
+  }
+}
+
+// ------------------------------------------------------------------ dK, dV pass
+template <int D>
+struct DkdvLayout {
+  static constexpr int kTile = BwdTiles<D>::kTile;
+  static constexpr int kOffK = 0;
+  static constexpr int kOffV = kTile;
+  static constexpr int kOffRing = 2 * kTile;      // stage s: Q_i, dO_i, lse2[128], D[128]
+  static constexpr int kStage = 2 * kTile + 1024;
+  static constexpr int kStages = 2;
+  static constexpr int kOffBar = kOffRing + kStages * kStage;
+  static constexpr int kNumBars = 13;
+  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffHolder + 8;
+  // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
+  // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
+  static constexpr int kUsed = kOffAbort + 8 + 1024;
+  static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+enum : int {
+  kKvFull = 0, kKvEmpty = 1, kQdFull = 2, kQdEmpty = 4, kSFull = 6, kDpFull = 7, kPFull = 8, kDsFull = 9,
+  kAccFull = 10, kAccEmpty = 11, kMmaDone = 12
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const BwdParams p) {
+  using Lay = DkdvLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + Lay::kOffBar + 8 * i; };
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + Lay::kOffAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Lay::kNumBars; ++i)
+      mbar_init(bar(i), (i == kPFull || i == kDsFull || i == kAccEmpty) ? 4 : 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + Lay::kOffHolder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kOffHolder);
+
+  const int nt = (p.N + BT - 1) / BT;
+  const int G = p.Hq / p.Hkv;
+  const int items = p.B * p.Hkv * nt;
+  // item it: key tile j = it / (B Hkv) (j = 0, the most query tiles under the causal rule, first)
+  auto item = [&](int it, int& b, int& hkv, int& j) {
+    j = it / (p.B * p.Hkv);
+    const int bk = it - j * p.B * p.Hkv;
+    b = bk / p.Hkv;
+    hkv = bk - b * p.Hkv;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t nkv = 0, nqd = 0;
+      const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        int b, hkv, j;
+        item(it, b, hkv, j);
+        if (!mbar_wait(bar(kKvEmpty), (nkv & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
+        mbar_arrive_expect_tx(bar(kKvFull), 2 * Lay::kTile);
+        load_tile<D>(sb + Lay::kOffK, &tk, bar(kKvFull), hkv, b * p.N + j * BT, pol_kv);
+        load_tile<D>(sb + Lay::kOffV, &tv, bar(kKvFull), hkv, b * p.N + j * BT, pol_kv);
+        ++nkv;
+        const int i0 = p.causal ? j : 0, ni = nt - i0;
+        for (int t = 0; t < G * ni; ++t) {
+          const int h = hkv * G + t / ni, i = i0 + t % ni;
+          const uint32_t st = nqd & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
+          if (!mbar_wait(bar(kQdEmpty + st), ((nqd >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kQdFull + st), 2 * Lay::kTile + 1024);
+          load_tile<D>(base, &tq, bar(kQdFull + st), h, b * p.N + i * BT, pol_q);
+          load_tile<D>(base + Lay::kTile, &tdo, bar(kQdFull + st), h, b * p.N + i * BT, pol_q);
+          const size_t vrow = (size_t)(b * p.Hq + h) * p.Npad + (size_t)i * BT;
+          bulk_load(base + 2 * Lay::kTile, p.ws_lse2 + vrow, 512, bar(kQdFull + st));
+          bulk_load(base + 2 * Lay::kTile + 512, p.ws_d + vrow, 512, bar(kQdFull + st));
+          ++nqd;
+        }
+      }
+      if (nkv) mbar_drain(bar(kKvFull), (nkv - 1) & 1);
+      for (uint32_t st = 0; st < 2; ++st) {
+        const uint32_t c = (nqd + 1 - st) / 2;
+        if (c) mbar_drain(bar(kQdFull + st), (c - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t nkv = 0, nqd = 0, np = 0, nds = 0, nacc = 0;
+      const uint64_t kd = smem_desc_sw128(sb + Lay::kOffK, 16, 1024);
+      const uint64_t vd = smem_desc_sw128(sb + Lay::kOffV, 16, 1024);
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDV = tmem + kColAcc, tDK = tmem + kColAcc + D;
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        int b, hkv, j;
+        item(it, b, hkv, j);
+        const int i0 = p.causal ? j : 0, steps = G * (nt - i0);
+        if (!mbar_wait(bar(kKvFull), nkv & 1, abort, p.status, kWaitLimitNs)) break;
+        ++nkv;
+        tc_fence_after();
+        for (int t = 0; t < steps; ++t) {
+          const uint32_t st = nqd & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
+          if (!mbar_wait(bar(kQdFull + st), (nqd >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t qk = smem_desc_sw128(base, 16, 1024), dok = smem_desc_sw128(base + Lay::kTile, 16, 1024);
+          const uint64_t qmn = smem_desc_sw128(base, BT * 128, 1024);
+          const uint64_t domn = smem_desc_sw128(base + Lay::kTile, BT * 128, 1024);
+          issue_kk<D>(tS, kd, qk);   // S^T = K Q^T (P^T of the previous step was read by its dV product)
+          mma_commit(bar(kSFull));
+          issue_kk<D>(tDP, vd, dok);  // dP^T = V dO^T (dS^T of the previous step was read by its dK product)
+          mma_commit(bar(kDpFull));
+          if (t == 0 && !mbar_wait(bar(kAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar(kPFull), np & 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ++np;
+          tc_fence_after();
+          issue_tn<D>(tDV, tS, domn, t > 0);  // dV += P^T dO
+          if (!mbar_wait(bar(kDsFull), nds & 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ++nds;
+          tc_fence_after();
+          issue_tn<D>(tDK, tDP, qmn, t > 0);  // dK += dS^T Q
+          mma_commit(bar(kQdEmpty + st));
+          ++nqd;
+        }
+        if (!ok) break;
+        mma_commit(bar(kKvEmpty));
+        mma_commit(bar(kAccFull));
+        ++nacc;
+      }
+      mma_commit(bar(kMmaDone));
+      mbar_drain(bar(kMmaDone), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ element-wise (one key row per thread)
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;                    // key row within the tile
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + kColS, dp_col = tmem + lane_off + kColDP;
+    const uint32_t dv_col = tmem + lane_off + kColAcc, dk_col = tmem + lane_off + kColAcc + D;
+    const float sl2 = p.scale * kLog2e;
+    uint32_t nqd = 0, ns = 0, ndp = 0, nacc = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      int b, hkv, j;
+      item(it, b, hkv, j);
+      const int i0 = p.causal ? j : 0, ni = nt - i0;
+      for (int t = 0; t < G * ni; ++t) {
+        const int i = i0 + t % ni;
+        const uint32_t st = nqd & 1;
+        const float* vec = reinterpret_cast<const float*>(smem + Lay::kOffRing + st * Lay::kStage + 2 * Lay::kTile);
+        if (!warp_wait(bar(kSFull), ns & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        ++ns;
+        // the stage's vectors arrived with its tiles, which S^T has consumed
+        mbar_try_wait(bar(kQdFull + st), (nqd >> 1) & 1);
+        tc_fence_after();
+        float pv[BT];
+        {
+          uint32_t u[BT];
+          tmem_ld128(s_col, u);
+          const bool diag = p.causal && i == j;       // queries before this key are masked
+#pragma unroll
+          for (int c = 0; c < BT; ++c) {
+            const float x = ex2(fmaf(__uint_as_float(u[c]), sl2, -vec[c]));
+            pv[c] = (diag && c < r) ? 0.f : x;
+          }
+        }
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {  // P^T in bf16 over the first 64 columns of S^T
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[64 * hh + 2 * c], pv[64 * hh + 2 * c + 1]);
+          tmem_st32(s_col + 32 * hh, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kPFull));
+        if (!warp_wait(bar(kDpFull), ndp & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        ++ndp;
+        tc_fence_after();
+        const float* dvec = vec + BT;
+        write_ds(dp_col, pv, [&](int c) { return dvec[c]; });
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kDsFull));
+        ++nqd;
+      }
+      if (!ok) break;
+      // epilogue: dV and scale * dK rows of this key tile
+      if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status)) break;
+      ++nacc;
+      tc_fence_after();
+      const int key = j * BT + r;
+      const bool live = key < p.N;
+      const size_t off = (((size_t)b * p.N + (live ? key : 0)) * p.Hkv + hkv) * D;
+      store_row<D>(dv_col, 1.f, static_cast<__nv_bfloat16*>(p.dv) + off, live);
+      store_row<D>(dk_col, p.scale, static_cast<__nv_bfloat16*>(p.dk) + off, live);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kAccEmpty));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ dQ pass
+template <int D>
+struct DqLayout {
+  static constexpr int kTile = BwdTiles<D>::kTile;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffDO = kTile;
+  static constexpr int kOffRing = 2 * kTile;      // stage s: K_j, V_j
+  static constexpr int kStage = 2 * kTile;
+  static constexpr int kStages = 2;
+  static constexpr int kOffBar = kOffRing + kStages * kStage;
+  static constexpr int kNumBars = 14;
+  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffHolder + 8;
+  // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
+  // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
+  static constexpr int kUsed = kOffAbort + 8 + 1024;
+  static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+enum : int {
+  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kQSFull = 6, kQSFree = 7, kQDpFull = 8, kQDsFull = 9,
+  kQAccFull = 10, kQAccEmpty = 11, kQMmaDone = 12
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdParams p) {
+  using Lay = DqLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sb = smem_u32(smem);
+  auto bar = [&](int i) -> uint32_t { return sb + Lay::kOffBar + 8 * i; };
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + Lay::kOffAbort);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < Lay::kNumBars; ++i)
+      mbar_init(bar(i), (i == kQSFree || i == kQDsFull || i == kQAccEmpty) ? 4 : 1);
+    *abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+  }
+  if (warp == 1) {
+    tmem_alloc(sb + Lay::kOffHolder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kOffHolder);
+
+  const int nt = (p.N + BT - 1) / BT;
+  const int G = p.Hq / p.Hkv;
+  const int items = p.B * p.Hq * nt;
+  // item it: query tile i = nt - 1 - it / (B Hq) (the most key tiles under the causal rule first)
+  auto item = [&](int it, int& b, int& h, int& i) {
+    const int k = it / (p.B * p.Hq);
+    const int bh = it - k * p.B * p.Hq;
+    i = nt - 1 - k;
+    b = bh / p.Hq;
+    h = bh - b * p.Hq;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t nq = 0, nkv = 0;
+      const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
+      bool ok = true;
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        int b, h, i;
+        item(it, b, h, i);
+        if (!mbar_wait(bar(kQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
+        mbar_arrive_expect_tx(bar(kQFull), 2 * Lay::kTile);
+        load_tile<D>(sb + Lay::kOffQ, &tq, bar(kQFull), h, b * p.N + i * BT, pol_q);
+        load_tile<D>(sb + Lay::kOffDO, &tdo, bar(kQFull), h, b * p.N + i * BT, pol_q);
+        ++nq;
+        const int jn = p.causal ? i + 1 : nt, hkv = h / G;
+        for (int j = 0; j < jn; ++j) {
+          const uint32_t st = nkv & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
+          if (!mbar_wait(bar(kKEmpty + st), ((nkv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kKFull + st), 2 * Lay::kTile);
+          load_tile<D>(base, &tk, bar(kKFull + st), hkv, b * p.N + j * BT, pol_kv);
+          load_tile<D>(base + Lay::kTile, &tv, bar(kKFull + st), hkv, b * p.N + j * BT, pol_kv);
+          ++nkv;
+        }
+      }
+      if (nq) mbar_drain(bar(kQFull), (nq - 1) & 1);
+      for (uint32_t st = 0; st < 2; ++st) {
+        const uint32_t c = (nkv + 1 - st) / 2;
+        if (c) mbar_drain(bar(kKFull + st), (c - 1) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // per key tile j: S_j = Q K_j^T, dP_j = dO V_j^T, then (once the element-wise
+    // warps have read S_j) S_{j+1}, then dQ += dS_j K_j.
+    if (lane == 0) {
+      uint32_t nq = 0, nkv = 0, nfree = 0, nds = 0, nacc = 0;
+      const uint64_t qd = smem_desc_sw128(sb + Lay::kOffQ, 16, 1024);
+      const uint64_t dod = smem_desc_sw128(sb + Lay::kOffDO, 16, 1024);
+      const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColAcc;
+      bool ok = true;
+      auto wait_kv = [&](uint32_t n) -> bool {
+        return mbar_wait(bar(kKFull + (n & 1)), (n >> 1) & 1, abort, p.status, kWaitLimitNs);
+      };
+      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+        int b, h, i;
+        item(it, b, h, i);
+        const int jn = p.causal ? i + 1 : nt;
+        if (!mbar_wait(bar(kQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
+        ++nq;
+        if (!wait_kv(nkv)) break;
+        tc_fence_after();
+        issue_kk<D>(tS, qd, smem_desc_sw128(sb + Lay::kOffRing + (nkv & 1) * Lay::kStage, 16, 1024));
+        mma_commit(bar(kQSFull));
+        for (int j = 0; j < jn; ++j) {
+          const uint32_t st = nkv & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
+          issue_kk<D>(tDP, dod, smem_desc_sw128(base + Lay::kTile, 16, 1024));  // dP = dO V_j^T
+          mma_commit(bar(kQDpFull));
+          if (j + 1 < jn) {
+            if (!wait_kv(nkv + 1) || !mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            ++nfree;
+            tc_fence_after();
+            issue_kk<D>(tS, qd, smem_desc_sw128(sb + Lay::kOffRing + ((nkv + 1) & 1) * Lay::kStage, 16, 1024));
+            mma_commit(bar(kQSFull));
+          }
+          if (j == 0 && !mbar_wait(bar(kQAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(bar(kQDsFull), nds & 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          ++nds;
+          tc_fence_after();
+          issue_tn<D>(tDQ, tDP, smem_desc_sw128(base, BT * 128, 1024), j > 0);  // dQ += dS K_j
+          mma_commit(bar(kKEmpty + st));
+          ++nkv;
+        }
+        if (!ok) break;
+        // the last S of the item was read before its dS was written
+        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs)) break;
+        ++nfree;
+        mma_commit(bar(kQEmpty));
+        mma_commit(bar(kQAccFull));
+        ++nacc;
+      }
+      mma_commit(bar(kQMmaDone));
+      mbar_drain(bar(kQMmaDone), 0);
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ element-wise (one query row per thread)
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_off + kColS, dp_col = tmem + lane_off + kColDP;
+    const uint32_t dq_col = tmem + lane_off + kColAcc;
+    const float sl2 = p.scale * kLog2e;
+    uint32_t ns = 0, ndp = 0, nacc = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      int b, h, i;
+      item(it, b, h, i);
+      const int jn = p.causal ? i + 1 : nt;
+      const int qrow = i * BT + r;
+      const size_t vrow = (size_t)(b * p.Hq + h) * p.Npad + qrow;
+      const float l2 = p.ws_lse2[vrow], dval = p.ws_d[vrow];
+      for (int j = 0; j < jn; ++j) {
+        if (!warp_wait(bar(kQSFull), ns & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        ++ns;
+        tc_fence_after();
+        float pv[BT];
+        {
+          uint32_t u[BT];
+          tmem_ld128(s_col, u);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kQSFree));  // S may be overwritten by the next tile's product
+          const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - j * BT;  // visible keys of this tile: c < lim
+#pragma unroll
+          for (int c = 0; c < BT; ++c) {
+            const float x = ex2(fmaf(__uint_as_float(u[c]), sl2, -l2));
+            pv[c] = c < lim ? x : 0.f;
+          }
+        }
+        if (!warp_wait(bar(kQDpFull), ndp & 1, abort, p.status)) {
+          ok = false;
+          break;
+        }
+        ++ndp;
+        tc_fence_after();
+        write_ds(dp_col, pv, [&](int) { return dval; });
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kQDsFull));
+      }
+      if (!ok) break;
+      if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status)) break;
+      ++nacc;
+      tc_fence_after();
+      const bool live = qrow < p.N;
+      const size_t off = (((size_t)b * p.N + (live ? qrow : 0)) * p.Hq + h) * D;
+      store_row<D>(dq_col, p.scale, static_cast<__nv_bfloat16*>(p.dq) + off, live);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQAccEmpty));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D>
+cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                         const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.Hq * p.Npad;
+  const int pre_blocks = (int)std::min<long long>((rows + 7) / 8, (long long)num_sms * 16);
+  bwd_preprocess_kernel<<<pre_blocks, 256, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const int nt = (p.N + BT - 1) / BT;
+  {
+    auto kern = bwd_dkdv_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::kBytes);
+    if (e != cudaSuccess) return e;
+    const long long items = (long long)p.B * p.Hkv * nt;
+    const int grid = (int)std::min<long long>(items, num_sms);
+    kern<<<grid, kThreads, DkdvLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  {
+    auto kern = bwd_dq_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::kBytes);
+    if (e != cudaSuccess) return e;
+    const long long items = (long long)p.B * p.Hq * nt;
+    const int grid = (int)std::min<long long>(items, num_sms);
+    kern<<<grid, kThreads, DqLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
+  if (p.d == 128) return launch_bwd_t<128>(p, tq, tk, tv, tdo, num_sms, stream);
+  return launch_bwd_t<64>(p, tq, tk, tv, tdo, num_sms, stream);
+}
+
+}  // namespace fattn

@@ -79,4 +79,28 @@ struct MergeParams {
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 
+// Attention backward (dense [B, N, H, d] bf16, lse [B, Hq, N] fp32 from the forward).
+struct BwdParams {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* ws_lse2;             // [B * Hq, Npad]: lse * log2(e), +inf past N
+  float* ws_d;                // [B * Hq, Npad]: rowsum(dO o O), 0 past N
+  int B, Hq, Hkv, N, d, Npad; // Npad = N rounded up to 128
+  int causal;
+  float scale;
+  int* status;
+};
+
+// Preprocess, dK/dV pass and dQ pass, in that order on `stream`. Tensor maps
+// are over the packed [B * N, H, d] views of q, k, v and dout (128-row boxes).
+cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, int num_sms, cudaStream_t stream);
+
 }  // namespace fattn

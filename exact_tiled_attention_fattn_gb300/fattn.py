@@ -34,6 +34,8 @@ SIGNATURES = {
     "fattn_fwd_block_sparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
     "fattn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                              _vp]),
+    "fattn_bwd_workspace_size": (_sz, [_i, _i, _i]),
+    "fattn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]),
     "fattn_decode_workspace_size": (_sz, [_i, _i, _i, _i]),
     "fattn_decode_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _f, _vp, _sz,
                                 _vp]),
@@ -239,6 +241,45 @@ def fwd_paged(q, kcache, vcache, block_table, seqlens_k, cu_seqlens_q, max_seqle
                              float(scale), ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_fwd_paged", st)
     return out, lse
+
+
+def bwd_workspace_size(B: int, Hq: int, N: int) -> int:
+    return int(load_library().fattn_bwd_workspace_size(B, Hq, N))
+
+
+def bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, dq=None, dk=None, dv=None,
+        workspace=None, stream=None):
+    """Attention backward. q, o, dout [B,N,Hq,d], k, v [B,N,Hkv,d] bf16; lse [B,Hq,N] fp32 from
+    ``fwd`` on the same inputs. Returns (dq, dk, dv) in the input layouts (bf16)."""
+    lib = load_library()
+    _need_cuda(q, k, v, o, lse, dout, dq, dk, dv, workspace)
+    if not (q.dtype == k.dtype == v.dtype == o.dtype == dout.dtype == torch.bfloat16):
+        raise TypeError("backward takes bf16 q, k, v, o and dout")
+    if q.dim() != 4 or k.dim() != 4:
+        raise ValueError("q must be [B, N, Hq, d] and k [B, N, Hkv, d]")
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    _expect(k, (B, N, Hkv, d), "k")
+    _expect(v, k.shape, "v")
+    _expect(o, q.shape, "o")
+    _expect(dout, q.shape, "dout")
+    _expect(lse, (B, Hq, N), "lse", torch.float32)
+    _expect(dq, q.shape, "dq", q.dtype)
+    _expect(dk, k.shape, "dk", q.dtype)
+    _expect(dv, k.shape, "dv", q.dtype)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_size(B, Hq, N)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    st = lib.fattn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv),
+                       B, Hq, Hkv, N, d, 1 if causal else 0, float(scale), _ptr(workspace),
+                       workspace.numel() * workspace.element_size(), ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_bwd", st)
+    return dq, dk, dv
 
 
 def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:

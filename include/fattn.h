@@ -145,6 +145,33 @@ fattn_status fattn_fwd_paged(const void* q, const void* kcache, const void* vcac
                              cudaStream_t stream);
 
 /*
+ * fattn_bwd_workspace_size — bytes of scratch fattn_bwd needs: two fp32
+ * arrays [B * Hq, Npad] (Npad = N rounded up to 128), each 256-byte aligned.
+ * Returns 0 for non-positive arguments.
+ */
+size_t fattn_bwd_workspace_size(int B, int Hq, int N);
+
+/*
+ * fattn_bwd — gradients of attention with respect to q, k and v.
+ * [FA-PAPER] "The backward pass recomputes instead of reading": P is rebuilt
+ * tile by tile from the saved logsumexp; D = rowsum(dO o O), dV = P^T dO,
+ * dP = dO V^T, dS = P o (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ *
+ * Dense layout, bf16: q, o, dout, dq [B, N, Hq, d]; k, v, dk, dv
+ * [B, N, Hkv, d]; lse [B, Hq, N] fp32 as written by fattn_fwd for the same
+ * q, k, v, causal and scale (o likewise). dk and dv sum over the Hq / Hkv
+ * query heads that share a KV head. All buffers are DEVICE memory.
+ * workspace: DEVICE, >= fattn_bwd_workspace_size(B, Hq, N) bytes, 256-byte
+ *   aligned, contents ignored; owned by the caller.
+ * Errors: INVALID_ARG (NULL or misaligned pointers, negative sizes,
+ *   Hq % Hkv != 0, non-finite scale), UNSUPPORTED (d not in {64, 128},
+ *   B * N or B * Hq * Npad >= 2^31), WORKSPACE (missing, small or misaligned).
+ */
+fattn_status fattn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                       const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N, int d,
+                       int causal, float scale, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * fattn_decode_workspace_size — bytes of scratch fattn_decode_paged needs:
  * the per-split partials lse_part [B, Hq, S] fp32 and o_part [B, Hq, S, d]
  * fp32 (S = num_splits), then 1 + B * Hq int32 work-scheduling counters, each

@@ -32,7 +32,8 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted(fattn.SIGNATURES), "binding signatures must mirror include/fattn.h"
     for n in names:
         assert hasattr(lib, n), n
-    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_paged", "fattn_decode_workspace_size",
+    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_paged", "fattn_bwd",
+                          "fattn_bwd_workspace_size", "fattn_decode_workspace_size",
                           "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
                           "fattn_debug_read_status"}
@@ -154,3 +155,21 @@ def test_paged_prefill_validation(lib):
     assert f(P=8) == E.FATTN_ERR_UNSUPPORTED and f(P=48) == E.FATTN_ERR_UNSUPPORTED
     assert f(pages=(1 << 31) // 16) == E.FATTN_ERR_UNSUPPORTED    # pool rows past int32
     assert f(Tq=0, q=None, bt=None) == E.FATTN_OK                  # empty problem
+
+
+def test_backward_validation(lib):
+    E = fattn
+    assert lib.fattn_bwd_workspace_size(2, 4, 300) == 2 * 2 * 4 * 384 * 4
+    assert lib.fattn_bwd_workspace_size(0, 4, 300) == 0
+
+    def f(**kw):
+        g = lambda n, dflt: kw.get(n, dflt)
+        return lib.fattn_bwd(g("q", A), A, A, A, A, A, A, A, A, g("B", 2), g("Hq", 4), g("Hkv", 2), g("N", 300),
+                             g("d", 128), 1, 0.1, g("ws", A), g("wsb", 1 << 20), None)
+    assert f(q=None) == E.FATTN_ERR_INVALID_ARG
+    assert f(Hkv=3) == E.FATTN_ERR_INVALID_ARG
+    assert f(d=96) == E.FATTN_ERR_UNSUPPORTED
+    assert f(ws=None) == E.FATTN_ERR_WORKSPACE
+    assert f(wsb=100) == E.FATTN_ERR_WORKSPACE
+    assert f(ws=A + 16) == E.FATTN_ERR_WORKSPACE
+    assert f(B=0, q=None) == E.FATTN_OK
