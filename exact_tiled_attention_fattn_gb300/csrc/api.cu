@@ -238,7 +238,7 @@ extern "C" fattn_status fattn_bwd(const void* q, const void* k, const void* v, c
   BwdParams p{};
   p.q = q; p.k = k; p.v = v; p.o = o; p.dout = dout; p.lse = lse;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  p.ws_lse2 = static_cast<float*>(workspace);
+  p.ws_nl2 = static_cast<float*>(workspace);
   p.ws_d = reinterpret_cast<float*>(static_cast<char*>(workspace) + need / 2);
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.Npad = (int)npad;
   p.causal = causal ? 1 : 0; p.scale = scale;

@@ -5,9 +5,11 @@
 //   dQ += scale dS K,    dK += scale dS^T Q     (S = scale Q K^T).
 //
 // Three launches on the caller's stream:
-//   bwd_preprocess_kernel  D and lse * log2(e) per query row, into a workspace
+//   bwd_preprocess_kernel  D and -lse * log2(e) per query row, into a workspace
 //                          padded to whole 128-row tiles (pad: D = 0,
-//                          lse = +inf, so padded rows get P = 0).
+//                          -lse log2(e) = -inf, so padded rows get P = 0);
+//                          then P = 2^(S log2(e) scale - lse log2(e)) is one
+//                          FMA and one exponential per element.
 //   bwd_dkdv_kernel<d>     one CTA per SM over items (sequence, KV head, 128-key
 //                          tile j); an item walks the query tiles i of every
 //                          query head sharing the KV head (causal: i >= j) and
@@ -23,8 +25,11 @@
 // accumulated with atomics from the dK/dV pass: at d = 128 the dK/dV pass
 // already uses all 512 TMEM columns (S^T, dP^T, dV, dK).
 //
-// Roles (256 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread),
-// warps 4-7 the element-wise work, one thread per TMEM lane (tile row).
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread),
+// warps 4-7 and 8-11 the element-wise work: a thread owns one TMEM lane (tile
+// row), warpgroup g columns [64 g, 64 g + 64) of it. Each warpgroup packs its
+// bf16 P or dS into the first 32 columns of its own 64, so the two never touch
+// each other's columns and the MMA reads its TMEM operand from the two halves.
 // Every pipeline wait is bounded as in the forward kernel: a wait past its
 // limit records FATTN_ERR_TIMEOUT, every role stops, copies and MMAs are
 // drained and TMEM is freed.
@@ -35,6 +40,7 @@
 #include <math_constants.h>
 
 #include <algorithm>
+#include <type_traits>
 
 namespace fattn {
 namespace {
@@ -42,7 +48,8 @@ namespace {
 using namespace sm100;
 
 constexpr int BT = 128;          // rows of every tile (query rows or keys)
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;   // warps 0-3 control, 4-7 and 8-11 element-wise
+constexpr int kEwArrivals = 8;  // element-wise warps arriving on a barrier
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
@@ -64,34 +71,100 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ------------------------------------------------------------------ preprocess
-// One warp per row of the padded [B * Hq, Npad] workspace.
+// Rows of O and dO in memory order ((b, i, h), each d contiguous), kRowsPerWarp
+// at a time per warp with their loads in flight together; each lane reads d / 32
+// elements of both. The padded workspace rows (i >= N) are written by a second loop.
+constexpr int kRowsPerWarp = 4;
+
+template <int D>
 __global__ void bwd_preprocess_kernel(const BwdParams p) {
+  constexpr int E = D / 32;  // elements per lane: 4 (8 bytes) or 2 (4 bytes)
+  using Vec = typename std::conditional<E == 4, uint2, uint32_t>::type;
   const int lane = threadIdx.x & 31;
-  const long long rows = (long long)p.B * p.Hq * p.Npad;
-  const long long warps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows; r += warps) {
-    const int bh = (int)(r / p.Npad), i = (int)(r - (long long)bh * p.Npad);
-    float dsum = 0.f, l2 = CUDART_INF_F;
-    if (i < p.N) {
-      const int b = bh / p.Hq, h = bh - b * p.Hq;
-      const size_t off = (((size_t)b * p.N + i) * p.Hq + h) * p.d;
-      const uint32_t* o2 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.o) + off);
-      const uint32_t* g2 = reinterpret_cast<const uint32_t*>(static_cast<const __nv_bfloat16*>(p.dout) + off);
-      for (int c = lane; c < p.d / 2; c += 32) {
-        const uint32_t a = __ldg(o2 + c), g = __ldg(g2 + c);
-        dsum = fmaf(bf16_lo(a), bf16_lo(g), dsum);
-        dsum = fmaf(bf16_hi(a), bf16_hi(g), dsum);
+  const int rows = p.B * p.N * p.Hq;               // < 2^31: checked on the host
+  const int warps = (int)((gridDim.x * blockDim.x) >> 5);
+  const int warp_id = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
+  const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout);
+  for (int m0 = warp_id * kRowsPerWarp; m0 < rows; m0 += warps * kRowsPerWarp) {
+    Vec a[kRowsPerWarp], d[kRowsPerWarp];
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      if (m0 + u < rows) {
+        const size_t off = (size_t)(m0 + u) * D + lane * E;
+        a[u] = __ldg(reinterpret_cast<const Vec*>(o + off));
+        d[u] = __ldg(reinterpret_cast<const Vec*>(g + off));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      const int m = m0 + u;
+      if (m >= rows) break;
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
+      const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d[u]);
+      float dsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < E / 2; ++w) {
+        dsum = fmaf(bf16_lo(aw[w]), bf16_lo(dw[w]), dsum);
+        dsum = fmaf(bf16_hi(aw[w]), bf16_hi(dw[w]), dsum);
       }
 #pragma unroll
       for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
-      const float lse = __ldg(p.lse + (size_t)bh * p.N + i);
-      if (lse > -CUDART_INF_F && lse < CUDART_INF_F) l2 = lse * kLog2e;  // a row with no key: P = 0
-    }
-    if (lane == 0) {
-      p.ws_lse2[r] = l2;
-      p.ws_d[r] = dsum;
+      if (lane == 0) {
+        const int h = m % p.Hq, bi = m / p.Hq;
+        const int i = bi % p.N, b = bi / p.N;
+        const int bh = b * p.Hq + h;
+        const float lse = __ldg(p.lse + (size_t)bh * p.N + i);
+        // a row with no visible key (lse = -inf) gets P = 0
+        p.ws_nl2[(size_t)bh * p.Npad + i] = (lse > -CUDART_INF_F && lse < CUDART_INF_F) ? -lse * kLog2e : -CUDART_INF_F;
+        p.ws_d[(size_t)bh * p.Npad + i] = dsum;
+      }
     }
   }
+  const int pad = p.Npad - p.N;
+  if (pad > 0) {
+    const int total = p.B * p.Hq * pad;
+    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
+      const int bh = t / pad, i = p.N + (t - bh * pad);
+      p.ws_nl2[(size_t)bh * p.Npad + i] = -CUDART_INF_F;  // padded query rows: P = 0
+      p.ws_d[(size_t)bh * p.Npad + i] = 0.f;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ work order
+// Items (head, tile) are taken in groups of heads whose items fill about two
+// rounds of the grid; inside a group the items go heaviest tile first (all heads
+// of the group at one tile index, then the next), and the grid walks the list in
+// alternating direction round by round ("snake"), so the tiles the CTAs stream
+// (Q and dO in the dK/dV pass, K and V in the dQ pass) belong to a few heads at
+// a time and are shared through L2. `unit` keeps GQA groups whole.
+struct BwdSchedule {
+  int tiles, heads, group, total;
+};
+__device__ __forceinline__ BwdSchedule make_bwd_schedule(int heads, int tiles, int unit) {
+  BwdSchedule s;
+  s.tiles = tiles;
+  s.heads = heads;
+  int grp = (2 * (int)gridDim.x + tiles - 1) / tiles;
+  grp = ((grp + unit - 1) / unit) * unit;
+  s.group = grp < heads ? grp : heads;
+  s.total = heads * tiles;
+  return s;
+}
+__device__ __forceinline__ int bwd_item_index(const BwdSchedule& s, int k) {
+  const int G = (int)gridDim.x;
+  const int idx = k * G + ((k & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+  return idx < s.total ? idx : -1;
+}
+// head and rank (0 = heaviest) of item it
+__device__ __forceinline__ void bwd_decode(const BwdSchedule& s, int it, int& head, int& rank) {
+  const int per_group = s.group * s.tiles;
+  const int g = it / per_group;
+  const int rem = it - g * per_group;
+  const int gh = min(s.group, s.heads - g * s.group);
+  rank = rem / gh;
+  head = g * s.group + (rem - rank * gh);
 }
 
 // ------------------------------------------------------------------ shared helpers
@@ -112,13 +185,15 @@ __device__ __forceinline__ void issue_kk(uint32_t d_tmem, uint64_t a0, uint64_t 
     mma_ss_c<true>(d_tmem, a0 + o, b0 + o, id);
   }
 }
-// D[tmem] (+)= A[tmem] B over 128 rows of B (B MN-major: the head dimension contiguous).
+// D[tmem] (+)= A[tmem] B over 128 rows of B (B MN-major: the head dimension contiguous);
+// A (bf16) in the two warpgroups' packed halves, columns [0, 32) and [64, 96).
 template <int D>
 __device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, bool acc) {
   constexpr uint32_t id = idesc_bf16_f32(BT, D, 1);
   mma_ts(d_tmem, a_tmem, b0, id, acc ? 1u : 0u);
 #pragma unroll
-  for (int ks = 1; ks < BT / 16; ++ks) mma_ts_acc(d_tmem, a_tmem + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), id);
+  for (int ks = 1; ks < BT / 16; ++ks)  // keys 64 g + 16 k' live at column 64 g + 8 k'
+    mma_ts_acc(d_tmem, a_tmem + (ks >> 2) * 64 + (ks & 3) * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), id);
 }
 
 // Load 128-row tile (rows r0.., head h) of a [rows, H, D] tensor map into dst.
@@ -147,25 +222,47 @@ __device__ __forceinline__ void store_row(uint32_t t_col, float mul, __nv_bfloat
   }
 }
 
-// dS = P o (dP - Dvec) for the 128 columns of this lane, written as bf16 over
-// the first 64 columns of the dP buffer, 32 columns at a time: pass q reads dP
-// columns [32q, 32q + 32) and then writes packed columns [16q, 16q + 16), all of
-// which the same or an earlier pass has already read.
-template <typename DAt>
-__device__ __forceinline__ void write_ds(uint32_t dp_col, const float (&pv)[BT], DAt dvec) {
+// dS = P o (dP - Dvec) over this warpgroup's 64 columns (pv[c] is column
+// 64 g + c), written as bf16 over the first 32 of them, 32 columns at a time:
+// pass q reads dP columns [32q, 32q + 32) and then writes packed columns
+// [16q, 16q + 16), all of which the same or an earlier pass has already read.
+template <bool kVecD>
+__device__ __forceinline__ void write_ds(uint32_t dp_col, const float (&pv)[64], const float* dvec, float dval) {
 #pragma unroll
-  for (int q = 0; q < BT / 32; ++q) {
+  for (int q = 0; q < 2; ++q) {
     uint32_t a[32];
     tmem_ld32(dp_col + 32 * q, a);
+    float dd[32];
+    if (kVecD) {  // D of each column (shared memory, 16-byte aligned)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float4 v = reinterpret_cast<const float4*>(dvec + 32 * q)[e];
+        dd[4 * e] = v.x;
+        dd[4 * e + 1] = v.y;
+        dd[4 * e + 2] = v.z;
+        dd[4 * e + 3] = v.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 32; ++e) dd[e] = dval;
+    }
     uint32_t w[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
       const int c = 32 * q + 2 * e;
-      w[e] = pack_bf16x2(pv[c] * (__uint_as_float(a[2 * e]) - dvec(c)),
-                         pv[c + 1] * (__uint_as_float(a[2 * e + 1]) - dvec(c + 1)));
+      w[e] = pack_bf16x2(pv[c] * (__uint_as_float(a[2 * e]) - dd[2 * e]),
+                         pv[c + 1] * (__uint_as_float(a[2 * e + 1]) - dd[2 * e + 1]));
     }
     tmem_st16(dp_col + 16 * q, w);
   }
+}
+
+// 64 consecutive fp32 TMEM columns of this lane.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
+  uint32_t (&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[0]);
+  uint32_t (&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&r[32]);
+  tmem_ld32(taddr, lo);
+  tmem_ld32(taddr + 32, hi);
 }
 
 // ------------------------------------------------------------------ dK, dV pass
@@ -174,7 +271,7 @@ struct DkdvLayout {
   static constexpr int kTile = BwdTiles<D>::kTile;
   static constexpr int kOffK = 0;
   static constexpr int kOffV = kTile;
-  static constexpr int kOffRing = 2 * kTile;      // stage s: Q_i, dO_i, lse2[128], D[128]
+  static constexpr int kOffRing = 2 * kTile;      // stage s: Q_i, dO_i, -lse log2(e) [128], D[128]
   static constexpr int kStage = 2 * kTile + 1024;
   static constexpr int kStages = 2;
   static constexpr int kOffBar = kOffRing + kStages * kStage;
@@ -207,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kPFull || i == kDsFull || i == kAccEmpty) ? 4 : 1);
+      mbar_init(bar(i), (i == kPFull || i == kDsFull || i == kAccEmpty) ? kEwArrivals : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -228,13 +325,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int nt = (p.N + BT - 1) / BT;
   const int G = p.Hq / p.Hkv;
-  const int items = p.B * p.Hkv * nt;
-  // item it: key tile j = it / (B Hkv) (j = 0, the most query tiles under the causal rule, first)
+  const BwdSchedule sch = make_bwd_schedule(p.B * p.Hkv, nt, 1);
+  // item: (sequence, KV head, key tile j); rank 0 = j 0, the most query tiles under the causal rule
   auto item = [&](int it, int& b, int& hkv, int& j) {
-    j = it / (p.B * p.Hkv);
-    const int bk = it - j * p.B * p.Hkv;
-    b = bk / p.Hkv;
-    hkv = bk - b * p.Hkv;
+    int head;
+    bwd_decode(sch, it, head, j);
+    b = head / p.Hkv;
+    hkv = head - b * p.Hkv;
   };
 
   if (warp == 0) {
@@ -243,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nkv = 0, nqd = 0;
       const uint64_t pol_kv = policy_evict_first(), pol_q = policy_evict_last();
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, hkv, j;
         item(it, b, hkv, j);
         if (!mbar_wait(bar(kKvEmpty), (nkv & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
@@ -263,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           load_tile<D>(base, &tq, bar(kQdFull + st), h, b * p.N + i * BT, pol_q);
           load_tile<D>(base + Lay::kTile, &tdo, bar(kQdFull + st), h, b * p.N + i * BT, pol_q);
           const size_t vrow = (size_t)(b * p.Hq + h) * p.Npad + (size_t)i * BT;
-          bulk_load(base + 2 * Lay::kTile, p.ws_lse2 + vrow, 512, bar(kQdFull + st));
+          bulk_load(base + 2 * Lay::kTile, p.ws_nl2 + vrow, 512, bar(kQdFull + st));
           bulk_load(base + 2 * Lay::kTile + 512, p.ws_d + vrow, 512, bar(kQdFull + st));
           ++nqd;
         }
@@ -282,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t vd = smem_desc_sw128(sb + Lay::kOffV, 16, 1024);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDV = tmem + kColAcc, tDK = tmem + kColAcc + D;
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, hkv, j;
         item(it, b, hkv, j);
         const int i0 = p.causal ? j : 0, steps = G * (nt - i0);
@@ -334,15 +431,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ element-wise (one key row per thread)
-    const int q4 = warp & 3;
+    const int q4 = warp & 3, wg = (warp - 4) >> 2;
     const int r = q4 * 32 + lane;                    // key row within the tile
+    const int cb = 64 * wg;                          // this warpgroup's query columns
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t s_col = tmem + lane_off + kColS, dp_col = tmem + lane_off + kColDP;
-    const uint32_t dv_col = tmem + lane_off + kColAcc, dk_col = tmem + lane_off + kColAcc + D;
+    const uint32_t s_col = tmem + lane_off + kColS + cb, dp_col = tmem + lane_off + kColDP + cb;
+    const uint32_t acc_col = tmem + lane_off + kColAcc + (wg ? D : 0);  // warpgroup 0 writes dV, 1 writes dK
     const float sl2 = p.scale * kLog2e;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t nqd = 0, ns = 0, ndp = 0, nacc = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+    for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
       int b, hkv, j;
       item(it, b, hkv, j);
       const int i0 = p.causal ? j : 0, ni = nt - i0;
@@ -358,23 +457,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the stage's vectors arrived with its tiles, which S^T has consumed
         mbar_try_wait(bar(kQdFull + st), (nqd >> 1) & 1);
         tc_fence_after();
-        float pv[BT];
+        float pv[64];
         {
-          uint32_t u[BT];
-          tmem_ld128(s_col, u);
+          uint32_t u[64];
+          tmem_ld64(s_col, u);
           const bool diag = p.causal && i == j;       // queries before this key are masked
+          const float4* nl = reinterpret_cast<const float4*>(vec + cb);  // -lse log2(e) per query column
 #pragma unroll
-          for (int c = 0; c < BT; ++c) {
-            const float x = ex2(fmaf(__uint_as_float(u[c]), sl2, -vec[c]));
-            pv[c] = (diag && c < r) ? 0.f : x;
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const float4 l = nl[c4];
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[4 * c4]), __uint_as_float(u[4 * c4 + 1])), sl2x2,
+                             f2_pack(l.x, l.y)), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[4 * c4 + 2]), __uint_as_float(u[4 * c4 + 3])), sl2x2,
+                             f2_pack(l.z, l.w)), x2, x3);
+            const int c = 4 * c4;
+            pv[c] = (diag && cb + c < r) ? 0.f : ex2(x0);
+            pv[c + 1] = (diag && cb + c + 1 < r) ? 0.f : ex2(x1);
+            pv[c + 2] = (diag && cb + c + 2 < r) ? 0.f : ex2(x2);
+            pv[c + 3] = (diag && cb + c + 3 < r) ? 0.f : ex2(x3);
           }
         }
+        {
+          uint32_t pk[32];  // P^T in bf16 over the first 32 of this warpgroup's S^T columns
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {  // P^T in bf16 over the first 64 columns of S^T
-          uint32_t pk[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[64 * hh + 2 * c], pv[64 * hh + 2 * c + 1]);
-          tmem_st32(s_col + 32 * hh, pk);
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(pv[2 * c], pv[2 * c + 1]);
+          tmem_st32(s_col, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -386,8 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ndp;
         tc_fence_after();
-        const float* dvec = vec + BT;
-        write_ds(dp_col, pv, [&](int c) { return dvec[c]; });
+        write_ds<true>(dp_col, pv, vec + BT + cb, 0.f);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -395,15 +502,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nqd;
       }
       if (!ok) break;
-      // epilogue: dV and scale * dK rows of this key tile
+      // epilogue: warpgroup 0 writes dV, warpgroup 1 scale * dK, one key row per thread
       if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status)) break;
       ++nacc;
       tc_fence_after();
       const int key = j * BT + r;
       const bool live = key < p.N;
       const size_t off = (((size_t)b * p.N + (live ? key : 0)) * p.Hkv + hkv) * D;
-      store_row<D>(dv_col, 1.f, static_cast<__nv_bfloat16*>(p.dv) + off, live);
-      store_row<D>(dk_col, p.scale, static_cast<__nv_bfloat16*>(p.dk) + off, live);
+      store_row<D>(acc_col, wg ? p.scale : 1.f, static_cast<__nv_bfloat16*>(wg ? p.dk : p.dv) + off, live);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kAccEmpty));
@@ -457,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kQSFree || i == kQDsFull || i == kQAccEmpty) ? 4 : 1);
+      mbar_init(bar(i), (i == kQSFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -478,14 +584,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int nt = (p.N + BT - 1) / BT;
   const int G = p.Hq / p.Hkv;
-  const int items = p.B * p.Hq * nt;
-  // item it: query tile i = nt - 1 - it / (B Hq) (the most key tiles under the causal rule first)
+  const BwdSchedule sch = make_bwd_schedule(p.B * p.Hq, nt, G);
+  // item: (sequence, query head, query tile i); rank 0 = the last tile, the most key tiles under the causal rule
   auto item = [&](int it, int& b, int& h, int& i) {
-    const int k = it / (p.B * p.Hq);
-    const int bh = it - k * p.B * p.Hq;
-    i = nt - 1 - k;
-    b = bh / p.Hq;
-    h = bh - b * p.Hq;
+    int head, rank;
+    bwd_decode(sch, it, head, rank);
+    i = nt - 1 - rank;
+    b = head / p.Hq;
+    h = head - b * p.Hq;
   };
 
   if (warp == 0) {
@@ -494,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nq = 0, nkv = 0;
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
       bool ok = true;
-      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, h, i;
         item(it, b, h, i);
         if (!mbar_wait(bar(kQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
@@ -534,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto wait_kv = [&](uint32_t n) -> bool {
         return mbar_wait(bar(kKFull + (n & 1)), (n >> 1) & 1, abort, p.status, kWaitLimitNs);
       };
-      for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+      for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, h, i;
         item(it, b, h, i);
         const int jn = p.causal ? i + 1 : nt;
@@ -585,21 +691,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ element-wise (one query row per thread)
-    const int q4 = warp & 3;
+    const int q4 = warp & 3, wg = (warp - 4) >> 2;
     const int r = q4 * 32 + lane;
+    const int cb = 64 * wg;                          // this warpgroup's key columns
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const uint32_t s_col = tmem + lane_off + kColS, dp_col = tmem + lane_off + kColDP;
+    const uint32_t s_col = tmem + lane_off + kColS + cb, dp_col = tmem + lane_off + kColDP + cb;
     const uint32_t dq_col = tmem + lane_off + kColAcc;
     const float sl2 = p.scale * kLog2e;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t ns = 0, ndp = 0, nacc = 0;
     bool ok = true;
-    for (int it = blockIdx.x; ok && it < items; it += gridDim.x) {
+    for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
       int b, h, i;
       item(it, b, h, i);
       const int jn = p.causal ? i + 1 : nt;
       const int qrow = i * BT + r;
       const size_t vrow = (size_t)(b * p.Hq + h) * p.Npad + qrow;
-      const float l2 = p.ws_lse2[vrow], dval = p.ws_d[vrow];
+      const float nl2 = p.ws_nl2[vrow], dval = p.ws_d[vrow];
+      const uint64_t nl2x2 = f2_pack(nl2, nl2);
       for (int j = 0; j < jn; ++j) {
         if (!warp_wait(bar(kQSFull), ns & 1, abort, p.status)) {
           ok = false;
@@ -607,18 +716,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ns;
         tc_fence_after();
-        float pv[BT];
+        float pv[64];
         {
-          uint32_t u[BT];
-          tmem_ld128(s_col, u);
+          uint32_t u[64];
+          tmem_ld64(s_col, u);
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(kQSFree));  // S may be overwritten by the next tile's product
-          const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - j * BT;  // visible keys of this tile: c < lim
+          // visible keys of this tile: column c < lim
+          const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - j * BT - cb;
 #pragma unroll
-          for (int c = 0; c < BT; ++c) {
-            const float x = ex2(fmaf(__uint_as_float(u[c]), sl2, -l2));
-            pv[c] = c < lim ? x : 0.f;
+          for (int c = 0; c < 64; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), sl2x2, nl2x2), x0, x1);
+            pv[c] = c < lim ? ex2(x0) : 0.f;
+            pv[c + 1] = c + 1 < lim ? ex2(x1) : 0.f;
           }
         }
         if (!warp_wait(bar(kQDpFull), ndp & 1, abort, p.status)) {
@@ -627,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         ++ndp;
         tc_fence_after();
-        write_ds(dp_col, pv, [&](int) { return dval; });
+        write_ds<false>(dp_col, pv, nullptr, dval);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -637,9 +749,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status)) break;
       ++nacc;
       tc_fence_after();
+      // warpgroup g writes columns [g D / 2, (g + 1) D / 2) of its row
       const bool live = qrow < p.N;
-      const size_t off = (((size_t)b * p.N + (live ? qrow : 0)) * p.Hq + h) * D;
-      store_row<D>(dq_col, p.scale, static_cast<__nv_bfloat16*>(p.dq) + off, live);
+      const size_t off = (((size_t)b * p.N + (live ? qrow : 0)) * p.Hq + h) * D + wg * (D / 2);
+      store_row<D / 2>(dq_col + wg * (D / 2), p.scale, static_cast<__nv_bfloat16*>(p.dq) + off, live);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kQAccEmpty));
@@ -657,9 +770,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.Hq * p.Npad;
-  const int pre_blocks = (int)std::min<long long>((rows + 7) / 8, (long long)num_sms * 16);
-  bwd_preprocess_kernel<<<pre_blocks, 256, 0, stream>>>(p);
+  const long long rows = (long long)p.B * p.N * p.Hq;
+  const long long per_block = 8LL * kRowsPerWarp;
+  const int pre_blocks = (int)std::min<long long>((rows + per_block - 1) / per_block, (long long)num_sms * 16);
+  bwd_preprocess_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -90,7 +90,7 @@ struct BwdParams {
   void* dq;
   void* dk;
   void* dv;
-  float* ws_lse2;             // [B * Hq, Npad]: lse * log2(e), +inf past N
+  float* ws_nl2;              // [B * Hq, Npad]: -lse * log2(e), -inf past N
   float* ws_d;                // [B * Hq, Npad]: rowsum(dO o O), 0 past N
   int B, Hq, Hkv, N, d, Npad; // Npad = N rounded up to 128
   int causal;
