@@ -46,11 +46,11 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sparse", action="store_true",
-                    help="skip the block-sparse and paged prefill measurements (outside the step)")
+                    help="skip the block-sparse, paged prefill and backward measurements (outside the step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--profile-once", action="store_true",
-                    help="one launch each of prefill, decode, block-sparse and paged prefill on the bench "
-                         "workloads, then exit (for ncu)")
+                    help="one launch each of prefill, decode, block-sparse prefill, paged prefill and "
+                         "backward on the bench workloads, then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -60,6 +60,8 @@ KERNEL_SOURCES = {
 }
 KERNEL_SOURCES["prefill_tc_kernel<128, sparse>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["prefill_tc_kernel<128, paged>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["bwd_dkdv_kernel<128>"] = ["backward.cu", "sm100_primitives.cuh", "device_common.cuh", "fattn_internal.h"]
+KERNEL_SOURCES["bwd_dq_kernel<128>"] = KERNEL_SOURCES["bwd_dkdv_kernel<128>"]
 
 
 def recorded_traffic(kernel: str):
@@ -245,6 +247,39 @@ def paged_prefill_leg(fattn, flush, stream, peaks, dev):
             "kv_bytes": kv, "traffic": recorded_traffic("prefill_tc_kernel<128, paged>")}
 
 
+def backward_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev):
+    """fattn_bwd on the prefill workload (dO ~ N(0, 1), seed 5; O and lse from fattn_fwd), 10 launches, median.
+    Work convention: 2.5 x the forward's FLOPs (five products of the forward's size, the usual count)."""
+    import torch
+    g = torch.Generator("cpu").manual_seed(5)
+    do = torch.randn(pre.q.shape, generator=g).to(torch.bfloat16).to(dev)
+    fattn.fwd(q, k, v, causal=True, scale=pre.scale, out=o, lse=lse)
+    B, N, Hq, _ = pre.q.shape
+    ws = torch.empty(fattn.bwd_workspace_size(B, Hq, N), dtype=torch.uint8, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    run = lambda: fattn.bwd(q, k, v, o, lse, do, causal=True, scale=pre.scale, dq=dq, dk=dk, dv=dv, workspace=ws)
+    for _ in range(3):
+        flush()
+        run()
+    ts = []
+    for _ in range(10):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    t = statistics.median(ts)
+    fl = 2.5 * pre.flops()
+    tf = fl / (t * 1e-3) / 1e12
+    return {"workload": "backward of the causal MHA prefill B=4 Hq=Hkv=32 N=4096 d=128 (preprocess + dK/dV + dQ "
+                        "launches)", "ms": t, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "flops": fl, "launches": 3,
+            "traffic": {"bwd_dkdv_kernel<128>": recorded_traffic("bwd_dkdv_kernel<128>"),
+                        "bwd_dq_kernel<128>": recorded_traffic("bwd_dq_kernel<128>")}}
+
+
 def cpu_baseline_prefill(pre, seconds: float):
     """Time the fp64 oracle on sampled query rows of the prefill workload."""
     import numpy as np
@@ -351,6 +386,9 @@ def main():
             x = paged_prefill_workload()            # and one paged (chunked) prefill launch
             pa = [t.to(dev) for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q)]
             fattn.fwd_paged(*pa, max(x.lengths_q), causal=True, scale=x.scale)
+            do = torch.randn(q.shape, device=dev).to(torch.bfloat16)  # and one backward
+            prefill()
+            fattn.bwd(q, k, v, o, lse, do, causal=True, scale=pre.scale)
         torch.cuda.synchronize()
         st = fattn.debug_read_status()
         print(json.dumps({"profile_once": True, "num_splits": S, "device_status": st}), flush=True)
@@ -465,6 +503,7 @@ def main():
 
     sparse = None if args.no_sparse else block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks)
     paged = None if args.no_sparse else paged_prefill_leg(fattn, flush, stream, peaks, dev)
+    backward = None if args.no_sparse else backward_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -503,6 +542,7 @@ def main():
         "prefill_ms": t_pre,
         "block_sparse": sparse,
         "paged_prefill": paged,
+        "backward": backward,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
