@@ -68,6 +68,7 @@ __all__ = [
     "decode_paged",
     "attn_fwd_paged",
     "attn_bwd",
+    "attn_fwd_masked",
     "decode_split_ranges",
     "decode_partials",
     "merge_partials",
@@ -117,13 +118,14 @@ def attention_weights(q, k, scale: float, causal: bool = False, rows=None) -> np
     return np.where(l[:, None] > 0, w / np.where(l > 0, l, 1.0)[:, None], 0.0)
 
 
-def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None, allowed=None):
+def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None, allowed=None, bias=None):
     """Exact attention for one head by the definition, fp64.
 
     q [Nq, d], k [Nk, d], v [Nk, dv]. Returns (O [r, dv], lse [r]) for the
     requested query rows (all by default), lse = m + ln(l) of the scaled,
     masked scores (natural log). ``allowed`` (bool [Nq, Nk]) further restricts
-    which keys each query sees (M = -inf where it is False).
+    which keys each query sees (M = -inf where it is False); ``bias`` ([Nq, Nk])
+    is the additive mask M of the formula, added to the scaled scores.
     """
     q = _f64(q)
     k = _f64(k)
@@ -136,6 +138,9 @@ def attention_definition(q, k, v, scale: float, causal: bool = False, rows=None,
     ok = _allowed(rows, nk, nq, causal)
     if allowed is not None:
         ok = ok & np.asarray(allowed, dtype=bool)[rows]
+    if bias is not None:                               # softmax(scale Q K^T + M)
+        s = s + _f64(bias)[rows]
+        ok = ok & np.isfinite(s)                       # M = -inf removes the key
     s = np.where(ok, s, -np.inf)
     m = s.max(axis=1)                                  # running-max target m
     finite = np.isfinite(m)
@@ -183,6 +188,42 @@ def attn_fwd(q, k, v, scale: float, causal: bool, cu_seqlens=None):
         for h in range(Hq):
             o[a:e, h], lse[h, a:e] = attention_definition(q[a:e, h], k[a:e, h // g],
                                                           v[a:e, h // g], scale, causal)
+    return o, lse
+
+
+def attn_fwd_masked(q, k, v, scale: float, causal: bool, mask, rows=None):
+    """Prefill with an additive mask, by the definition ([FA-LLM] formula
+    O = softmax(Q K^T / sqrt(d) + M) V).
+
+    Dense q [B, N, Hq, d], k/v [B, N, Hkv, d]; mask broadcastable to
+    [B, Hq, N, N] (leading dimensions of size 1 are shared), added to the scaled
+    scores; entries of -inf remove keys, and with ``causal`` the causal rule
+    applies on top. A row left with no key has O = 0, lse = -inf.
+    Returns O [B, N, Hq, d], lse [B, Hq, N]; with rows (int [n, 3] of
+    (b, h, i)) only those: O [n, d], lse [n].
+    """
+    q = _f64(q)
+    k = _f64(k)
+    v = _f64(v)
+    m = _f64(mask)
+    B, N, Hq, _ = q.shape
+    g = Hq // k.shape[2]
+    mb = lambda b, h: m[b if m.shape[0] > 1 else 0, h if m.shape[1] > 1 else 0]
+    if rows is not None:
+        rows = np.asarray(rows, dtype=np.int64)
+        o = np.zeros((len(rows), v.shape[-1]))
+        lse = np.zeros(len(rows))
+        for n, (b, h, i) in enumerate(rows):
+            ob, lb = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
+                                          rows=[int(i)], bias=mb(b, h))
+            o[n], lse[n] = ob[0], lb[0]
+        return o, lse
+    o = np.zeros(q.shape[:3] + (v.shape[-1],))
+    lse = np.zeros((B, Hq, N))
+    for b in range(B):
+        for h in range(Hq):
+            o[b, :, h], lse[b, h] = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale,
+                                                         causal, bias=mb(b, h))
     return o, lse
 
 

@@ -527,3 +527,50 @@ def test_backward_closed_form_uniform_causal():
     kr = _rand(rng, B, N, H, d)
     dq, dk, _ = orc.attn_bwd(q, kr, vc, do, 0.5, False)
     assert np.max(np.abs(dq)) <= 1e-13 and np.max(np.abs(dk)) <= 1e-13
+
+
+def test_additive_mask_vs_python_loops():
+    """O = softmax(scale Q K^T + M) V with a general additive M (-inf entries remove keys)."""
+    rng = np.random.default_rng(50)
+    B, N, Hq, Hkv, d, sc = 2, 7, 2, 1, 3, 0.6
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    m = 2.0 * _rand(rng, 1, Hq, N, N)
+    m[0, 1, 3, [0, 2, 5]] = -np.inf
+    m[0, 0, 4, :] = -np.inf                                  # row 4 of head 0 sees nothing
+    for causal in (False, True):
+        o, lse = orc.attn_fwd_masked(q, k, v, sc, causal, m)
+        for b in range(B):
+            for h in range(Hq):
+                for i in range(N):
+                    keys = [j for j in range(N) if np.isfinite(m[0, h, i, j]) and (not causal or j <= i)]
+                    if not keys:
+                        assert np.all(o[b, i, h] == 0) and np.isneginf(lse[b, h, i])
+                        continue
+                    s = [sc * float(q[b, i, h] @ k[b, j, 0]) + m[0, h, i, j] for j in keys]
+                    mx = max(s)
+                    w = [math.exp(x - mx) for x in s]
+                    tot = sum(w)
+                    ref = sum(wi * v[b, j, 0] for wi, j in zip(w, keys)) / tot
+                    assert np.max(np.abs(o[b, i, h] - ref)) <= 1e-13
+                    assert abs(lse[b, h, i] - (mx + math.log(tot))) <= 1e-13
+
+
+def test_additive_mask_special_cases():
+    rng = np.random.default_rng(51)
+    B, N, H, d, sc = 1, 9, 2, 4, 0.5
+    q, k, v = _rand(rng, B, N, H, d), _rand(rng, B, N, H, d), _rand(rng, B, N, H, d)
+    o0, l0 = orc.attn_fwd(q, k, v, sc, False)
+    o1, l1 = orc.attn_fwd_masked(q, k, v, sc, False, np.zeros((1, 1, N, N)))
+    assert np.array_equal(o0, o1) and np.array_equal(l0, l1)          # M = 0 is no mask
+    tri = np.where(np.tril(np.ones((N, N))) > 0, 0.0, -np.inf)[None, None]
+    oc, lc = orc.attn_fwd(q, k, v, sc, True)
+    o2, l2 = orc.attn_fwd_masked(q, k, v, sc, False, tri)
+    assert np.max(np.abs(o2 - oc)) <= 1e-15 and np.max(np.abs(l2 - lc)) <= 1e-15  # -inf above the diagonal = causal
+    c = rng.normal(size=(1, H, N, 1)) * 3                             # a per-row constant shifts lse only
+    o3, l3 = orc.attn_fwd_masked(q, k, v, sc, False, np.broadcast_to(c, (1, H, N, N)))
+    assert np.max(np.abs(o3 - o0)) <= 1e-13
+    assert np.max(np.abs(l3 - (l0 + c[0, :, :, 0][None]))) <= 1e-13
+    smp = np.array([[0, 1, 3], [0, 0, 8]])
+    os_, ls_ = orc.attn_fwd_masked(q, k, v, sc, False, tri, rows=smp)
+    for n, (b, h, i) in enumerate(smp):
+        assert np.max(np.abs(os_[n] - o2[b, i, h])) <= 1e-15 and abs(ls_[n] - l2[b, h, i]) <= 1e-15
