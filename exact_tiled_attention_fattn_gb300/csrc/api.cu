@@ -165,6 +165,42 @@ extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, con
   return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
+extern "C" fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                         int Hq, int Hkv, int N, int d, int causal, float scale, const void* mask,
+                                         long long mask_batch_stride, long long mask_head_stride,
+                                         int mask_row_stride, cudaStream_t stream) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o || !mask) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(mask)) return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  // whole 16-byte groups of 8 entries: every stride a multiple of 8, rows at least N long
+  if (mask_row_stride < N || mask_row_stride % 8 || mask_batch_stride < 0 || mask_batch_stride % 8 ||
+      mask_head_stride < 0 || mask_head_stride % 8)
+    return FATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * N;
+  if (rows > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+
+  int err = 0;
+  PrefillParams p{};
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
+  p.causal = causal ? 1 : 0; p.scale = scale;
+  p.mask_heads = 1;
+  p.mask = mask; p.mask_sb = mask_batch_stride; p.mask_sh = mask_head_stride; p.mask_ld = mask_row_stride;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
+      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+    return FATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
+
 extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const void* vcache,
                                         const int32_t* block_table, const int32_t* seqlens_k,
                                         const int32_t* cu_seqlens_q, void* o, float* lse, int B, int Hq, int Hkv,

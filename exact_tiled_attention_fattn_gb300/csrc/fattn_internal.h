@@ -34,6 +34,11 @@ struct PrefillParams {
   const int32_t* block_table; // device [B][max_pages]; nullptr = K/V in q's row space
   const int32_t* seqlens_k;   // device [B]: context tokens per sequence (>= its queries)
   int page_size, max_pages, num_pages;
+  // masked variant only: additive bf16 mask, entry (b, h, i, j) at
+  // mask[b * mask_sb + h * mask_sh + i * mask_ld + j] (strides in elements, multiples of 8)
+  const void* mask;           // nullptr = none
+  long long mask_sb, mask_sh;
+  int mask_ld;
 };
 
 // Longest mask row (blocks) the block-sparse kernel holds in shared memory.

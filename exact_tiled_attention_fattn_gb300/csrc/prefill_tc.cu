@@ -238,10 +238,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok;
 }
 
-template <int D, bool kSparse, bool kPaged>
+// Variants of the kernel (template argument kMode).
+enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3 };
+
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+  constexpr bool kSparse = kMode == kModeSparse;  // fixed block mask, zero blocks skipped
+  constexpr bool kPaged = kMode == kModePaged;    // K/V through a block table
+  constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
   using Lay = TcLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -676,8 +682,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m = -CUDART_INF_F, l = 0.f;
       bool first = true;
+      // additive mask: this row's entries (bf16), row clamped into the sequence (rows past it are not written)
+      const __nv_bfloat16* mrow = nullptr;
+      if constexpr (kMasked)
+        mrow = static_cast<const __nv_bfloat16*>(p.mask) + (size_t)x.b * p.mask_sb + (size_t)x.h * p.mask_sh +
+               (size_t)min(row, x.L - 1) * p.mask_ld;
       BitWalk walk(mw, 1 << t, x.n[t]);
       for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < x.n[t]; j = kSparse ? walk.next() : j + 1) {
+        // the tile's 128 mask entries, requested before waiting for S (16-byte loads
+        // of whole 8-key groups; groups at or past the visible limit are not read)
+        uint4 mv[kMasked ? BN / 8 : 1];
+        if constexpr (kMasked) {
+#pragma unroll
+          for (int c8 = 0; c8 < BN / 8; ++c8)
+            mv[c8] = j * BN + 8 * c8 < lim ? __ldg(reinterpret_cast<const uint4*>(mrow + j * BN + 8 * c8))
+                                           : make_uint4(0u, 0u, 0u, 0u);
+        }
         if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status)) {
           ok = false;
           break;
@@ -685,15 +705,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++ns;
         tc_fence_after();
         float s[BN];
-        {
-          uint32_t u[BN];
-          tmem_ld128(s_col, u);
-#pragma unroll
-          for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(u[e]);
-        }
         const int kbase = j * BN;
-        const bool masked = kbase + BN > lim;  // causal diagonal tile or sequence end
-        if (masked) {
+        bool masked = kbase + BN > lim;  // causal diagonal tile or sequence end
+        if constexpr (kMasked) {
+          // scores to the log2 domain with the mask added, s scale log2(e) + M log2(e),
+          // 32 columns at a time so each mask word dies as its scores arrive; keys past
+          // the visible limit -inf (their p is 0 below)
+#pragma unroll
+          for (int q32 = 0; q32 < BN / 32; ++q32) {
+            uint32_t u[32];
+            tmem_ld32(s_col + 32 * q32, u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const int c = 32 * q32 + e;
+              const uint4& g = mv[c >> 3];
+              const uint32_t w = ((c & 7) >> 1) == 0 ? g.x : ((c & 7) >> 1) == 1 ? g.y : ((c & 7) >> 1) == 2 ? g.z : g.w;
+              const float mval = (c & 1) ? bf16_hi(w) : bf16_lo(w);
+              s[c] = kbase + c < lim ? fmaf(__uint_as_float(u[e]), sl2, mval * kLog2e) : -CUDART_INF_F;
+            }
+          }
+          masked = false;
+        } else {
+          {
+            uint32_t u[BN];
+            tmem_ld128(s_col, u);
+#pragma unroll
+            for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(u[e]);
+          }
+        }
+        if (!kMasked && masked) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (kbase + c >= lim) s[c] = neg ? CUDART_INF_F : -CUDART_INF_F;
@@ -704,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float a[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) a[i] = s[i];
-          if (!neg) {
+          if (kMasked || !neg) {
 #pragma unroll
             for (int c = 8; c < BN; c += 16)
 #pragma unroll
@@ -718,19 +758,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fminf(a[6], a[7]));
           }
         }
-        const float m_cand = fmaxf(m, mx * sl2);
+        const float m_cand = fmaxf(m, kMasked ? mx : mx * sl2);  // the masked scores are already scaled
         const bool need = m_cand > m + kLazyRescaleLog2;          // always true on the first tile
         const float m_new = __any_sync(0xffffffffu, need) ? m_cand : m;
         const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
         const float alpha = ex2(m - base);                        // 1 when m is kept
         const uint64_t nbase2 = f2_pack(-base, -base);
+        const uint64_t mul2 = kMasked ? f2_pack(1.f, 1.f) : sl2x2;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[BN / 2];
         if (!masked) {
 #pragma unroll
           for (int c = 0; c < BN; c += 2) {
             float a0, a1;
-            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
+            f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, nbase2), a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
             acc[(c >> 1) & 7] += p0 + p1;
             pk[c / 2] = pack_bf16x2(p0, p1);
@@ -777,7 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++no;
       tc_fence_after();
       const bool live = row < x.L;
-      const float inv = 1.f / l;
+      // a row the mask left with no key: O = 0, lse = -inf
+      const float inv = (kMasked && l == 0.f) ? 0.f : 1.f / l;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -794,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (live && p.lse) {
-        const float lse = (m + log2f(l)) * kLn2;
+        const float lse = (kMasked && l == 0.f) ? -CUDART_INF_F : (m + log2f(l)) * kLn2;
         if (p.cu_seqlens)
           p.lse[(size_t)x.h * p.total_rows + x.row0 + row] = lse;
         else
@@ -811,11 +853,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kSparse, bool kPaged>
+template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      int num_sms, cudaStream_t stream) {
   using Lay = TcLayout<D>;
-  auto kern = prefill_tc_kernel<D, kSparse, kPaged>;
+  auto kern = prefill_tc_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
   const long long pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
@@ -831,15 +873,19 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
                               const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
   if (p.block_mask) {
-    if (p.d == 128) return launch_t<128, true, false>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, true, false>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, kModeSparse>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, kModeSparse>(p, tq, tk, tv, num_sms, stream);
   }
   if (p.block_table) {
-    if (p.d == 128) return launch_t<128, false, true>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, false, true>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, kModePaged>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, kModePaged>(p, tq, tk, tv, num_sms, stream);
   }
-  if (p.d == 128) return launch_t<128, false, false>(p, tq, tk, tv, num_sms, stream);
-  return launch_t<64, false, false>(p, tq, tk, tv, num_sms, stream);
+  if (p.mask) {
+    if (p.d == 128) return launch_t<128, kModeMasked>(p, tq, tk, tv, num_sms, stream);
+    return launch_t<64, kModeMasked>(p, tq, tk, tv, num_sms, stream);
+  }
+  if (p.d == 128) return launch_t<128, kModeDense>(p, tq, tk, tv, num_sms, stream);
+  return launch_t<64, kModeDense>(p, tq, tk, tv, num_sms, stream);
 }
 
 }  // namespace fattn

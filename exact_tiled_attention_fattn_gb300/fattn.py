@@ -32,6 +32,8 @@ _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_
 SIGNATURES = {
     "fattn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _i, _vp]),
     "fattn_fwd_block_sparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
+    "fattn_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, ctypes.c_longlong,
+                              ctypes.c_longlong, _i, _vp]),
     "fattn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                              _vp]),
     "fattn_bwd_workspace_size": (_sz, [_i, _i, _i]),
@@ -202,6 +204,42 @@ def fwd_block_sparse(q, k, v, block_mask, causal: bool = False, scale: float | N
                                     1 if causal else 0, float(scale), _ptr(block_mask), block_mask.shape[0],
                                     ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_fwd_block_sparse", st)
+    return out, lse
+
+
+def fwd_masked(q, k, v, mask, causal: bool = False, scale: float | None = None, out=None, lse=None,
+               want_lse: bool = True, stream=None):
+    """Prefill with an additive bf16 mask: O = softmax(scale Q K^T + M) V.
+    q [B,N,Hq,d], k/v [B,N,Hkv,d] bf16; mask [Bm, Hm, N, L] bf16 on the device with
+    Bm in {1, B}, Hm in {1, Hq} (size 1 is shared) and row length L >= N, L a multiple of 8
+    (entries past N are ignored). Returns (O, lse [B,Hq,N]); a row with no key gets
+    O = 0, lse = -inf."""
+    lib = load_library()
+    _need_cuda(q, k, v, mask, out, lse)
+    if not (q.dtype == k.dtype == v.dtype == mask.dtype == torch.bfloat16):
+        raise TypeError("masked prefill takes bf16 q, k, v and mask")
+    if q.dim() != 4 or k.dim() != 4 or mask.dim() != 4:
+        raise ValueError("q [B,N,Hq,d], k [B,N,Hkv,d] and mask [Bm,Hm,N,L] expected")
+    B, N, Hq, d = q.shape
+    _expect(k, (B, N, k.shape[2], d), "k")
+    _expect(v, k.shape, "v")
+    _expect(out, q.shape, "out", q.dtype)
+    _expect(lse, (B, Hq, N), "lse", torch.float32)
+    Bm, Hm, Nm, L = mask.shape
+    if Bm not in (1, B) or Hm not in (1, Hq) or Nm != N or L < N or L % 8:
+        raise ValueError(f"mask must be [1 or {B}, 1 or {Hq}, {N}, L] with L >= {N}, L % 8 == 0")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    sb = 0 if Bm == 1 else Hm * N * L
+    sh = 0 if Hm == 1 else N * L
+    st = lib.fattn_fwd_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, k.shape[2], N, d,
+                              1 if causal else 0, float(scale), _ptr(mask), sb, sh, L,
+                              ctypes.c_void_p(_stream_handle(stream)))
+    _check("fattn_fwd_masked", st)
     return out, lse
 
 

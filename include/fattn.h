@@ -111,6 +111,28 @@ fattn_status fattn_fwd_block_sparse(const void* q, const void* k, const void* v,
                                     const uint8_t* block_mask, int mask_heads, cudaStream_t stream);
 
 /*
+ * fattn_fwd_masked — prefill with a general additive mask M.
+ * [FA-LLM] the formula O = softmax(Q K^T / sqrt(d) + M) V ("The trick: tiles
+ * and an online softmax": M is added to each score tile while it is on chip).
+ *
+ * Dense layout and bf16, as fattn_fwd: q, o [B, N, Hq, d]; k, v [B, N, Hkv, d];
+ * lse [B, Hq, N] (may be NULL).
+ * mask: DEVICE bf16; entry (b, h, i, j) (query head h, query i, key j) is
+ *   mask[b * mask_batch_stride + h * mask_head_stride + i * mask_row_stride + j]
+ *   (strides in elements; 0 shares one mask over the batch or the heads). It is
+ *   added to the scaled scores; -inf removes the key. With causal != 0 the
+ *   causal rule applies on top. A row left with no key gets O = 0, lse = -inf.
+ *   Entries at keys >= N are not read.
+ * Errors: those of fattn_fwd (bf16, d in {64, 128}); INVALID_ARG for a NULL or
+ *   misaligned (16 bytes) mask, mask_row_stride < N, or a stride that is negative
+ *   or not a multiple of 8.
+ */
+fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int Hq, int Hkv, int N, int d, int causal, float scale,
+                              const void* mask, long long mask_batch_stride, long long mask_head_stride,
+                              int mask_row_stride, cudaStream_t stream);
+
+/*
  * fattn_fwd_paged — prefill of query chunks against a paged KV cache
  * (chunked prefill, or a whole prompt read back from the cache).
  * [FA-LLM] "Paged variants" (the tiled computation with K/V read through a

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert names == sorted(fattn.SIGNATURES), "binding signatures must mirror include/fattn.h"
     for n in names:
         assert hasattr(lib, n), n
-    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_paged", "fattn_bwd",
+    assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_masked", "fattn_fwd_paged", "fattn_bwd",
                           "fattn_bwd_workspace_size", "fattn_decode_workspace_size",
                           "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
@@ -173,3 +173,19 @@ def test_backward_validation(lib):
     assert f(wsb=100) == E.FATTN_ERR_WORKSPACE
     assert f(ws=A + 16) == E.FATTN_ERR_WORKSPACE
     assert f(B=0, q=None) == E.FATTN_OK
+
+
+def test_masked_validation(lib):
+    E = fattn
+
+    def f(**kw):
+        g = lambda n, dflt: kw.get(n, dflt)
+        return lib.fattn_fwd_masked(g("q", A), A, A, A, None, g("B", 2), 4, 2, g("N", 300), g("d", 128), 1, 0.1,
+                                    g("m", A), g("sb", 0), g("sh", 0), g("ld", 304), None)
+    assert f(m=None) == E.FATTN_ERR_INVALID_ARG
+    assert f(m=A + 8) == E.FATTN_ERR_INVALID_ARG
+    assert f(ld=296) == E.FATTN_ERR_INVALID_ARG          # shorter than N
+    assert f(ld=302) == E.FATTN_ERR_INVALID_ARG          # not whole groups of 8
+    assert f(sb=12) == E.FATTN_ERR_INVALID_ARG and f(sh=-8) == E.FATTN_ERR_INVALID_ARG
+    assert f(d=96) == E.FATTN_ERR_UNSUPPORTED
+    assert f(B=0, q=None, m=None) == E.FATTN_OK
