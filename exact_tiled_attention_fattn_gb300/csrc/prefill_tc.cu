@@ -636,6 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale * kLog2e;      // scores go to the log2 domain
     const bool neg = sl2 < 0.f;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
+    const uint64_t scale2 = f2_pack(p.scale, p.scale);
     uint32_t ns = 0, no = 0;                 // S_t and O_t completions seen
     uint32_t nm = 0;                         // block-mask slots consumed
     bool ok = true;
@@ -708,21 +709,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kbase = j * BN;
         bool masked = kbase + BN > lim;  // causal diagonal tile or sequence end
         if constexpr (kMasked) {
-          // scores to the log2 domain with the mask added, s scale log2(e) + M log2(e),
-          // 32 columns at a time so each mask word dies as its scores arrive; keys past
-          // the visible limit -inf (their p is 0 below)
+          // masked scores s scale + M (natural-log units; log2(e) is applied with the
+          // exponent), one packed FMA per column pair, 32 columns at a time so each
+          // mask word dies as its scores arrive; keys past the visible limit -inf
+          // (their p is 0 below)
 #pragma unroll
           for (int q32 = 0; q32 < BN / 32; ++q32) {
             uint32_t u[32];
             tmem_ld32(s_col + 32 * q32, u);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
+            for (int e = 0; e < 32; e += 2) {
               const int c = 32 * q32 + e;
               const uint4& g = mv[c >> 3];
               const uint32_t w = ((c & 7) >> 1) == 0 ? g.x : ((c & 7) >> 1) == 1 ? g.y : ((c & 7) >> 1) == 2 ? g.z : g.w;
-              const float mval = (c & 1) ? bf16_hi(w) : bf16_lo(w);
-              s[c] = kbase + c < lim ? fmaf(__uint_as_float(u[e]), sl2, mval * kLog2e) : -CUDART_INF_F;
+              float t0, t1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), scale2,
+                               f2_pack(bf16_lo(w), bf16_hi(w))), t0, t1);
+              s[c] = t0;
+              s[c + 1] = t1;
             }
+          }
+          if (masked) {
+#pragma unroll
+            for (int c = 0; c < BN; ++c)
+              if (kbase + c >= lim) s[c] = -CUDART_INF_F;
           }
           masked = false;
         } else {
@@ -758,13 +768,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mx = fmin3(fmin3(a[0], a[1], a[2]), fmin3(a[3], a[4], a[5]), fminf(a[6], a[7]));
           }
         }
-        const float m_cand = fmaxf(m, kMasked ? mx : mx * sl2);  // the masked scores are already scaled
+        const float m_cand = fmaxf(m, mx * (kMasked ? kLog2e : sl2));  // the masked scores carry the scale
         const bool need = m_cand > m + kLazyRescaleLog2;          // always true on the first tile
         const float m_new = __any_sync(0xffffffffu, need) ? m_cand : m;
         const float base = m_new == -CUDART_INF_F ? 0.f : m_new;
         const float alpha = ex2(m - base);                        // 1 when m is kept
         const uint64_t nbase2 = f2_pack(-base, -base);
-        const uint64_t mul2 = kMasked ? f2_pack(1.f, 1.f) : sl2x2;
+        const uint64_t mul2 = kMasked ? f2_pack(kLog2e, kLog2e) : sl2x2;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         uint32_t pk[BN / 2];
         if (!masked) {
