@@ -332,6 +332,41 @@ def prefill_paged(seed: int, B: int, Hq: int, Hkv: int, d: int, page_size: int,
                               page_size, causal, s, lengths_q, lengths_k, spare_pages)
 
 
+@dataclass
+class Fp8Inputs:
+    """Dense FP8 (E4M3) prefill inputs with per-tensor descale factors:
+    x = descale * e4m3(x8). q8 [B, N, Hq, d], k8/v8 [B, N, Hkv, d] as uint8 codes."""
+
+    q8: torch.Tensor
+    k8: torch.Tensor
+    v8: torch.Tensor
+    q_descale: float
+    k_descale: float
+    v_descale: float
+    causal: bool
+    scale: float
+
+    def flops(self) -> float:
+        B, N, Hq, d = self.q8.shape
+        f = 4.0 * B * Hq * N * N * d
+        return f / 2 if self.causal else f
+
+
+def prefill_fp8(seed: int, B: int, N: int, Hq: int, Hkv: int, d: int, causal: bool,
+                scale: float | None = None) -> Fp8Inputs:
+    """Q, K, V iid N(0, 1) (draw order Q, K, V), each quantized to E4M3 with the
+    per-tensor descale amax / 448 (the largest finite E4M3 value)."""
+    g = torch.Generator("cpu").manual_seed(seed)
+    xs = [_randn(g, (B, N, Hq, d)), _randn(g, (B, N, Hkv, d)), _randn(g, (B, N, Hkv, d))]
+    codes, descales = [], []
+    for x in xs:
+        ds = float(x.abs().max()) / 448.0
+        codes.append((x / ds).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
+        descales.append(ds)
+    s = 1.0 / math.sqrt(d) if scale is None else scale
+    return Fp8Inputs(codes[0], codes[1], codes[2], descales[0], descales[1], descales[2], causal, s)
+
+
 # ---- the five workloads (shapes of the pages' problems; sizes fixed here) ----
 
 def tiny_config(dtype: torch.dtype = torch.float32) -> PrefillInputs:

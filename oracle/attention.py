@@ -69,6 +69,8 @@ __all__ = [
     "attn_fwd_paged",
     "attn_bwd",
     "attn_fwd_masked",
+    "e4m3_to_f64",
+    "attn_fwd_fp8",
     "decode_split_ranges",
     "decode_partials",
     "merge_partials",
@@ -225,6 +227,33 @@ def attn_fwd_masked(q, k, v, scale: float, causal: bool, mask, rows=None):
             o[b, :, h], lse[b, h] = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale,
                                                          causal, bias=mb(b, h))
     return o, lse
+
+
+def e4m3_to_f64(codes) -> np.ndarray:
+    """Decode FP8 E4M3 bytes (the 'fn' variant: 1 sign bit, 4 exponent bits with
+    bias 7, 3 mantissa bits, subnormals at exponent 0, no infinities, S.1111.111
+    = NaN) to float64, from the bit layout."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 0x7).astype(np.float64)
+    val = np.where(e == 0, m / 8.0 * 2.0 ** (1 - 7), (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7))
+    val = np.where((e == 0xF) & ((c & 0x7) == 0x7), np.nan, val)
+    return sign * val
+
+
+def attn_fwd_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float, scale: float, causal: bool,
+                 rows=None):
+    """FP8 prefill ([FA-LLM] family table, FlashAttention-3: FP8 inputs): the
+    definition on the dequantized inputs Q = q_descale * dec(q8), K, V likewise.
+    q8 [B, N, Hq, d], k8/v8 [B, N, Hkv, d] E4M3 bytes (uint8). Returns O, lse as
+    attn_fwd, or at sampled rows (int [n, 3] of (b, h, i))."""
+    q = e4m3_to_f64(q8) * q_descale
+    k = e4m3_to_f64(k8) * k_descale
+    v = e4m3_to_f64(v8) * v_descale
+    if rows is None:
+        return attn_fwd(q, k, v, scale, causal)
+    return attn_fwd_rows(q, k, v, scale, causal, rows)
 
 
 def attn_fwd_rows(q, k, v, scale: float, causal: bool, samples, cu_seqlens=None):

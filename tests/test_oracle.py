@@ -574,3 +574,42 @@ def test_additive_mask_special_cases():
     os_, ls_ = orc.attn_fwd_masked(q, k, v, sc, False, tri, rows=smp)
     for n, (b, h, i) in enumerate(smp):
         assert np.max(np.abs(os_[n] - o2[b, i, h])) <= 1e-15 and abs(ls_[n] - l2[b, h, i]) <= 1e-15
+
+
+def test_e4m3_decode_closed_forms():
+    """E4M3 ('fn'): bias 7, 3 mantissa bits, subnormals, no infinities, 0x7f / 0xff NaN."""
+    dec = orc.e4m3_to_f64
+    assert dec([0x38])[0] == 1.0 and dec([0xB8])[0] == -1.0
+    assert dec([0x7E])[0] == 448.0 and dec([0xFE])[0] == -448.0        # largest finite
+    assert dec([0x08])[0] == 2.0 ** -6                                    # smallest normal
+    assert dec([0x01])[0] == 2.0 ** -9 and dec([0x07])[0] == 7 * 2.0 ** -9  # subnormals
+    assert dec([0x00])[0] == 0.0 and dec([0x80])[0] == 0.0
+    assert np.isnan(dec([0x7F])[0]) and np.isnan(dec([0xFF])[0])
+    assert dec([0x3C])[0] == 1.5 and dec([0x44])[0] == 3.0 and dec([0x78])[0] == 256.0
+    v = dec(np.arange(256))
+    fin = np.isfinite(v)
+    assert fin.sum() == 254 and len(np.unique(v[fin])) == 253             # +0 and -0 coincide
+
+
+def test_e4m3_decode_agrees_with_torch():
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).double().numpy()
+    mine = orc.e4m3_to_f64(codes.numpy())
+    assert np.array_equal(np.isnan(mine), np.isnan(ref))
+    assert np.array_equal(mine[~np.isnan(mine)], ref[~np.isnan(ref)])
+
+
+def test_fp8_attention_is_the_definition_on_dequantized_inputs():
+    from exact_tiled_attention_fattn_gb300 import inputs
+    x = inputs.prefill_fp8(60, 1, 40, 2, 1, 16, True)
+    o, lse = orc.attn_fwd_fp8(x.q8, x.k8, x.v8, x.q_descale, x.k_descale, x.v_descale, x.scale, True)
+    q = orc.e4m3_to_f64(x.q8.numpy()) * x.q_descale
+    k = orc.e4m3_to_f64(x.k8.numpy()) * x.k_descale
+    v = orc.e4m3_to_f64(x.v8.numpy()) * x.v_descale
+    for h in range(2):
+        for i in (0, 17, 39):
+            o_ref, l_ref = _python_attention([q[0, i, h].tolist()], k[0, : i + 1, 0].tolist(), v[0, : i + 1, 0].tolist(),
+                                             x.scale, False)
+            assert np.max(np.abs(o[0, i, h] - o_ref[0])) <= 1e-12 and abs(lse[0, h, i] - l_ref[0]) <= 1e-12
+    assert abs(np.max(np.abs(q)) - 448 * x.q_descale) <= 1e-9 * np.max(np.abs(q))  # amax scaled to 448
