@@ -64,6 +64,22 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int rows, int H, int d,
   return r == CUDA_SUCCESS;
 }
 
+// 3-D view of one-byte elements (E4M3) [d2][d1][d0] with row strides s1, s2
+// (bytes), box b0 x b1 x b2, 128-byte swizzle. Elements past the view read as zero.
+bool encode_u8_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
+                   uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = get_encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {s1, s2};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int num_sms_current() {  // declared in fattn_internal.h
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -244,6 +260,57 @@ extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+extern "C" size_t fattn_fwd_fp8_workspace_size(int B, int Hkv, int N, int d) {
+  if (B <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return 0;
+  const size_t npad = ((size_t)N + 127) / 128 * 128;
+  return align256((size_t)B * Hkv * d * npad);
+}
+
+extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                                      int Hkv, int N, int d, int causal, float scale, float q_descale,
+                                      float k_descale, float v_descale, void* workspace, size_t workspace_bytes,
+                                      cudaStream_t stream) {
+  if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
+  if (B == 0 || N == 0) return FATTN_OK;
+  if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || !std::isfinite(scale)) return FATTN_ERR_INVALID_ARG;
+  if (!(q_descale > 0.f) || !(k_descale > 0.f) || !(v_descale > 0.f) || !std::isfinite(q_descale) ||
+      !std::isfinite(k_descale) || !std::isfinite(v_descale))
+    return FATTN_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return FATTN_ERR_INVALID_ARG;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
+  if (d != 128) return FATTN_ERR_UNSUPPORTED;
+  const long long rows = (long long)B * N;
+  const long long npad = ((long long)N + 127) / 128 * 128;
+  if (rows > 0x7fffffffLL || npad > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
+  const size_t need = fattn_fwd_fp8_workspace_size(B, Hkv, N, d);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return FATTN_ERR_WORKSPACE;
+
+  int err = 0;
+  PrefillParams p{};
+  p.q = q; p.k = k; p.v = workspace; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
+  p.causal = causal ? 1 : 0;
+  p.scale = scale * q_descale * k_descale;  // S = scale (q_descale Q8)(k_descale K8)^T
+  p.mask_heads = 1;
+  p.fp8 = 1;
+  p.v_descale = v_descale;
+  p.status = status_ptr(&err);
+  if (err) return FATTN_ERR_CUDA;
+  uint8_t* vt = static_cast<uint8_t*>(workspace);
+  if (launch_fp8_transpose_v(static_cast<const uint8_t*>(v), vt, B, N, Hkv, d, (int)npad, stream) != cudaSuccess)
+    return FATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!encode_u8_map(&tq, q, d, Hq, rows, (uint64_t)d, (uint64_t)Hq * d, 128, 1, 128) ||
+      !encode_u8_map(&tk, k, d, Hkv, rows, (uint64_t)d, (uint64_t)Hkv * d, 128, 1, 128) ||
+      !encode_u8_map(&tv, vt, npad, d, (uint64_t)B * Hkv, (uint64_t)npad, (uint64_t)npad * d, 128, 128, 1))
+    return FATTN_ERR_CUDA;
+  const int sms = num_sms_current();
+  if (sms <= 0) return FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+}
 
 extern "C" size_t fattn_bwd_workspace_size(int B, int Hq, int N) {
   if (B <= 0 || Hq <= 0 || N <= 0) return 0;

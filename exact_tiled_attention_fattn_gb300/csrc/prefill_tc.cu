@@ -45,6 +45,7 @@
 #include "fattn_internal.h"
 #include "sm100_primitives.cuh"
 
+#include <cuda_fp8.h>
 #include <math_constants.h>
 
 namespace fattn {
@@ -86,10 +87,11 @@ constexpr int kMaskSlotBytes = 2 * kMaskWords * 4 + 16;
 constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8 softmax warps
 static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
-template <int D>
+template <int D, bool kFp8 = false>
 struct TcLayout {
-  static constexpr int kQBytes = BM * D * 2;      // one Q tile
-  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kElem = kFp8 ? 1 : 2;      // bytes per Q/K/V element (E4M3 or bf16)
+  static constexpr int kQBytes = BM * D * kElem;  // one Q tile
+  static constexpr int kKVBytes = BN * D * kElem;
   static constexpr int kStages = 2;
   static constexpr int kOffQ = 0;                 // Q_A then Q_B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
@@ -99,11 +101,15 @@ struct TcLayout {
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffMask = kOffAbort + 8;  // block-mask ring (block-sparse variant)
+  // FP8 variant: P_A, P_B as E4M3 128 x 128 tiles in shared memory (128-byte swizzle)
+  static constexpr int kOffP = (kOffMask + kMaskSlots * kMaskSlotBytes + 1023) / 1024 * 1024;
+  static constexpr int kPBytes = kFp8 ? BM * BN : 0;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would block in tcgen05.alloc) never shares the SM
-  static constexpr int kUsed = kOffMask + kMaskSlots * kMaskSlotBytes + 1024;
+  static constexpr int kUsed = kOffP + 2 * kPBytes + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
-  // TMEM columns: fp32 scores S_A, S_B (P_X in bf16 over their first 64 columns), fp32 O_A, O_B.
+  // TMEM columns: fp32 scores S_A, S_B (bf16 variants: P_X in bf16 over their first 64
+  // columns), fp32 O_A, O_B.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
   static_assert(256 + 2 * D <= kTmemCols, "TMEM budget");
@@ -239,7 +245,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Variants of the kernel (template argument kMode).
-enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3 };
+enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
 
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -248,7 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kSparse = kMode == kModeSparse;  // fixed block mask, zero blocks skipped
   constexpr bool kPaged = kMode == kModePaged;    // K/V through a block table
   constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
-  using Lay = TcLayout<D>;
+  constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V^T; P in E4M3 through shared memory
+  static_assert(!kFp8 || D == 128, "FP8 tiles are 128 one-byte columns: one 128-byte swizzle span");
+  constexpr int kChunks = kFp8 ? 1 : D / 64;      // 128-byte boxes per tile row
+  using Lay = TcLayout<D, kFp8>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -321,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t)
 #pragma unroll
-            for (int dc = 0; dc < D / 64; ++dc)
+            for (int dc = 0; dc < kChunks; ++dc)
               tma_load_3d(sb + Lay::kOffQ + t * Lay::kQBytes + dc * BM * 128, &tq, bar(kBarQFull), dc * 64, x.h,
                           x.row0 + x.base + t * BM, pol_q);
         }
@@ -331,7 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block table, each entry checked); slots past the sequence's last page read a
         // box beyond the pool, which the copy fills with zeros. The boxes stack into the
         // same swizzled layout as one 128-row box (page_size is a multiple of 8 rows).
-        auto issue_kv = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j) {
+        auto issue_kv = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j, bool is_v) {
+          if constexpr (kFp8) {
+            if (is_v) {  // V^T tile: head-dim rows, 128 keys per row, from the transposed copy
+              tma_load_3d(dst, map, full, j * BN, 0, x.b * p.Hkv + hkv, pol_kv);
+              return;
+            }
+          }
           if constexpr (kPaged) {
             const int P = p.page_size, per = BN / P;  // per <= 8 (page_size >= 16)
             const int i = lane;                       // this lane's page of the tile
@@ -351,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           } else {
 #pragma unroll
-            for (int dc = 0; dc < D / 64; ++dc)
+            for (int dc = 0; dc < kChunks; ++dc)
               tma_load_3d(dst + dc * BN * 128, map, full, dc * 64, hkv, x.row0 + j * BN, pol_kv);
           }
         };
@@ -360,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
           // a lane's copy may complete before the leader's expect: the phase still needs the leader's arrival
           if (leader) mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
-          issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j);
+          issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j, false);
           ++nk;
           return true;
         };
@@ -368,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t st = nv & 1;
           if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
           if (leader) mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
-          issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j);
+          issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j, true);
           ++nv;
           return true;
         };
@@ -415,11 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd1 = smem_desc_sw128(sb + Lay::kOffQ + Lay::kQBytes, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sb + Lay::kOffK, 16, 1024);
       const uint64_t kd1 = smem_desc_sw128(sb + Lay::kOffK + Lay::kKVBytes, 16, 1024);
-      const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, BN * 128, 1024);
-      const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, BN * 128, 1024);
+      // V: MN-major (d contiguous) for bf16; the FP8 variant holds V^T, K-major
+      const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, kFp8 ? 16 : BN * 128, 1024);
+      const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, kFp8 ? 16 : BN * 128, 1024);
       auto issue_s = [&](int t, uint32_t kst) {
         const uint32_t d_tmem = tmem + Lay::col_s(t);
         const uint64_t a0 = t ? qd1 : qd0, b0 = kst ? kd1 : kd0;
+        if constexpr (kFp8) {  // K = 32 one-byte elements (32 bytes) per instruction
+          constexpr uint32_t idS8 = idesc_e4m3_f32(BM, BN);
+          mma_ss_e4m3<false>(d_tmem, a0, b0, idS8);
+#pragma unroll
+          for (int ks = 1; ks < D / 32; ++ks) mma_ss_e4m3<true>(d_tmem, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 2), idS8);
+          mma_commit(bar(kBarSFull + t));
+          return;
+        }
         mma_ss_c<false>(d_tmem, a0, b0, idS);
 #pragma unroll
         for (int ks = 1; ks < D / 16; ++ks) {
@@ -435,6 +459,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t p_tmem = tmem + Lay::col_s(t), o_tmem = tmem + Lay::col_o(t);
         const uint64_t b0 = vst ? vd1 : vd0;
+        if constexpr (kFp8) {  // O += P V with P (E4M3, shared memory) and V^T both K-major
+          constexpr uint32_t idO8 = idesc_e4m3_f32(BM, D);
+          const uint64_t a0 = smem_desc_sw128(sb + Lay::kOffP + t * Lay::kPBytes, 16, 1024);
+          mma_ss_e4m3_p(o_tmem, a0, b0, idO8, acc ? 1u : 0u);
+#pragma unroll
+          for (int ks = 1; ks < BN / 32; ++ks) mma_ss_e4m3<true>(o_tmem, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 2), idO8);
+          return true;
+        }
         mma_ts(o_tmem, p_tmem, b0, idO, acc ? 1u : 0u);
 #pragma unroll
         for (int ks = 1; ks < BN / 16; ++ks) mma_ts_acc(o_tmem, p_tmem + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), idO);
@@ -776,6 +808,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t nbase2 = f2_pack(-base, -base);
         const uint64_t mul2 = kMasked ? f2_pack(kLog2e, kLog2e) : sl2x2;
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // a column pair of P: bf16x2, or (FP8 variant) E4M3x2 in the low 16 bits
+        auto pack_p = [](float p0, float p1) -> uint32_t {
+          if constexpr (kFp8)
+            return (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(p0, p1), __NV_SATFINITE, __NV_E4M3);
+          else
+            return pack_bf16x2(p0, p1);
+        };
         uint32_t pk[BN / 2];
         if (!masked) {
 #pragma unroll
@@ -784,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, nbase2), a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
             acc[(c >> 1) & 7] += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
+            pk[c / 2] = pack_p(p0, p1);
           }
         } else {
           const int vis = lim - kbase;
@@ -794,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
             const float p0 = c < vis ? ex2(a0) : 0.f, p1 = c + 1 < vis ? ex2(a1) : 0.f;
             acc[(c >> 1) & 7] += p0 + p1;
-            pk[c / 2] = pack_bf16x2(p0, p1);
+            pk[c / 2] = pack_p(p0, p1);
           }
         }
         const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -812,7 +851,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m = m_new;
         first = false;
-        tmem_st64(s_col, pk);
+        if constexpr (kFp8) {
+          // P in E4M3 (p <= 2^8 < 448, the largest finite value), row r of the tile's
+          // 128 x 128-byte buffer, 16-byte chunk c at chunk position c ^ (r mod 8) (the
+          // 128-byte swizzle the descriptor declares). P_t's previous product has
+          // completed: it was issued before S_t(j), whose completion this thread saw.
+          uint8_t* prow = smem + Lay::kOffP + t * Lay::kPBytes + r * 128;
+#pragma unroll
+          for (int c16 = 0; c16 < 8; ++c16) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)  // pk[i]: the E4M3 pair of columns 2i, 2i + 1
+              w[e] = pk[8 * c16 + 2 * e] | (pk[8 * c16 + 2 * e + 1] << 16);
+            *reinterpret_cast<uint4*>(prow + ((c16 ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          fence_proxy_async_smem();
+        } else {
+          tmem_st64(s_col, pk);
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -829,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool live = row < x.L;
       // a row the mask left with no key: O = 0, lse = -inf
-      const float inv = (kMasked && l == 0.f) ? 0.f : 1.f / l;
+      const float inv = (kMasked && l == 0.f) ? 0.f : (kFp8 ? p.v_descale : 1.f) / l;
       __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -866,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      int num_sms, cudaStream_t stream) {
-  using Lay = TcLayout<D>;
+  using Lay = TcLayout<D, kMode == kModeFp8>;
   auto kern = prefill_tc_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
@@ -890,6 +946,7 @@ cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, con
     if (p.d == 128) return launch_t<128, kModePaged>(p, tq, tk, tv, num_sms, stream);
     return launch_t<64, kModePaged>(p, tq, tk, tv, num_sms, stream);
   }
+  if (p.fp8) return p.d == 128 ? launch_t<128, kModeFp8>(p, tq, tk, tv, num_sms, stream) : cudaErrorInvalidValue;
   if (p.mask) {
     if (p.d == 128) return launch_t<128, kModeMasked>(p, tq, tk, tv, num_sms, stream);
     return launch_t<64, kModeMasked>(p, tq, tk, tv, num_sms, stream);
