@@ -46,11 +46,12 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sparse", action="store_true",
-                    help="skip the block-sparse, paged prefill and backward measurements (outside the step)")
+                    help="skip the block-sparse, paged, masked and FP8 prefill and backward measurements "
+                         "(outside the step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
     ap.add_argument("--profile-once", action="store_true",
-                    help="one launch each of prefill, decode, block-sparse prefill, paged prefill and "
-                         "backward on the bench workloads, then exit (for ncu)")
+                    help="one launch each of prefill, decode, block-sparse, paged, masked and FP8 prefill "
+                         "and backward on the bench workloads, then exit (for ncu)")
     return ap.parse_args()
 
 
@@ -60,6 +61,8 @@ KERNEL_SOURCES = {
 }
 KERNEL_SOURCES["prefill_tc_kernel<128, sparse>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["prefill_tc_kernel<128, paged>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["prefill_tc_kernel<128, masked>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["prefill_tc_kernel<128, fp8>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["bwd_dkdv_kernel<128>"] = ["backward.cu", "sm100_primitives.cuh", "device_common.cuh", "fattn_internal.h"]
 KERNEL_SOURCES["bwd_dq_kernel<128>"] = KERNEL_SOURCES["bwd_dkdv_kernel<128>"]
 
@@ -280,6 +283,62 @@ def backward_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev):
                         "bwd_dq_kernel<128>": recorded_traffic("bwd_dq_kernel<128>")}}
 
 
+def _time_launches(run, flush, stream, n=10):
+    import torch
+    for _ in range(3):
+        flush()
+        run()
+    ts = []
+    for _ in range(n):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        run()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def alibi_mask(N: int, dev):
+    """One shared bf16 additive mask [1, 1, N, N]: M[i, j] = -0.01 (i - j)."""
+    import torch
+    i = torch.arange(N, dtype=torch.float32, device=dev)
+    return (-0.01 * (i[:, None] - i[None, :])).to(torch.bfloat16)[None, None].contiguous()
+
+
+def masked_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev):
+    """fattn_fwd_masked on the prefill inputs with one shared ALiBi-style bias, causal."""
+    m = alibi_mask(pre.q.shape[1], dev)
+    t = _time_launches(lambda: fattn.fwd_masked(q, k, v, m, causal=True, scale=pre.scale, out=o, lse=lse), flush,
+                       stream)
+    tf = pre.flops() / (t * 1e-3) / 1e12
+    return {"workload": "causal MHA B=4 Hq=Hkv=32 N=4096 d=128 + one shared bf16 bias M[i,j] = -0.01 (i - j)",
+            "ms": t, "tflops": tf, "frac_of_bf16_peak": tf / peaks["bf16_tflops"],
+            "traffic": recorded_traffic("prefill_tc_kernel<128, masked>")}
+
+
+def fp8_leg(fattn, pre, flush, stream, peaks, dev):
+    """fattn_fwd_fp8 on E4M3 inputs of the prefill workload's shape (seed 1, per-tensor descales)."""
+    import torch
+    from exact_tiled_attention_fattn_gb300 import inputs
+    B, N, Hq, d = pre.q.shape
+    x = inputs.prefill_fp8(1, B, N, Hq, pre.hkv, d, True)
+    q8, k8, v8 = x.q8.to(dev), x.k8.to(dev), x.v8.to(dev)
+    ws = torch.empty(int(fattn.load_library().fattn_fwd_fp8_workspace_size(B, pre.hkv, N, d)), dtype=torch.uint8,
+                     device=dev)
+    o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    t = _time_launches(lambda: fattn.fwd_fp8(q8, k8, v8, x.q_descale, x.k_descale, x.v_descale, causal=True,
+                                             scale=x.scale, out=o, lse=lse, workspace=ws), flush, stream)
+    tf = x.flops() / (t * 1e-3) / 1e12
+    peak8 = 2.0 * peaks["bf16_tflops"]   # the measured bf16 peak x the nominal fp8 : bf16 ratio (4.5 : 2.25)
+    return {"workload": "causal MHA B=4 Hq=Hkv=32 N=4096 d=128, E4M3 q, k, v (per-tensor descales), bf16 O; "
+                        "V transpose launch included", "ms": t, "tflops": tf, "peak_fp8_tflops": peak8,
+            "peak_source": "measured bf16_tflops x 2 (nominal fp8/bf16 ratio)", "frac_of_fp8_peak": tf / peak8,
+            "launches": 2, "traffic": recorded_traffic("prefill_tc_kernel<128, fp8>")}
+
+
 def cpu_baseline_prefill(pre, seconds: float):
     """Time the fp64 oracle on sampled query rows of the prefill workload."""
     import numpy as np
@@ -386,6 +445,11 @@ def main():
             x = paged_prefill_workload()            # and one paged (chunked) prefill launch
             pa = [t.to(dev) for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q)]
             fattn.fwd_paged(*pa, max(x.lengths_q), causal=True, scale=x.scale)
+            fattn.fwd_masked(q, k, v, alibi_mask(pre.q.shape[1], dev), causal=True, scale=pre.scale)  # masked
+            from exact_tiled_attention_fattn_gb300 import inputs
+            x8 = inputs.prefill_fp8(1, *pre.q.shape[:3], pre.hkv, pre.q.shape[3], True)  # and FP8
+            fattn.fwd_fp8(x8.q8.to(dev), x8.k8.to(dev), x8.v8.to(dev), x8.q_descale, x8.k_descale, x8.v_descale,
+                          causal=True, scale=x8.scale)
             do = torch.randn(q.shape, device=dev).to(torch.bfloat16)  # and one backward
             prefill()
             fattn.bwd(q, k, v, o, lse, do, causal=True, scale=pre.scale)
@@ -504,6 +568,8 @@ def main():
     sparse = None if args.no_sparse else block_sparse_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks)
     paged = None if args.no_sparse else paged_prefill_leg(fattn, flush, stream, peaks, dev)
     backward = None if args.no_sparse else backward_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev)
+    masked = None if args.no_sparse else masked_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev)
+    fp8 = None if args.no_sparse else fp8_leg(fattn, pre, flush, stream, peaks, dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -543,6 +609,8 @@ def main():
         "block_sparse": sparse,
         "paged_prefill": paged,
         "backward": backward,
+        "masked_prefill": masked,
+        "fp8_prefill": fp8,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "clocks": clocks,
