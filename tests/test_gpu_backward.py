@@ -47,3 +47,23 @@ def test_backward_parity(fa, B, N, Hq, Hkv, d, causal):
         assert np.all(np.isfinite(as_np(a)))
         assert mx <= 2e-2 * max(1.0, rmax), f"{name}: max err {mx:.3e} (ref max {rmax:.3f})"
         assert mean <= 4e-3 * max(rmean, 1e-3), f"{name}: mean err {mean:.3e} (ref mean {rmean:.3f})"
+
+
+def test_backward_full_size_sampled_heads(fa):
+    """The bench's workload (causal MHA B=4 H=32 N=4096 d=128) in the launch the bench times; the
+    oracle's gradients for three whole (sequence, head) slices, every row."""
+    x = inputs.causal_mha_config()
+    B, N, H, d = x.q.shape
+    g = torch.Generator("cpu").manual_seed(5)
+    do = torch.randn((B, N, H, d), generator=g).to(torch.bfloat16)
+    q, k, v, dog = x.q.cuda(), x.k.cuda(), x.v.cuda(), do.cuda()
+    o, lse = fa.fwd(q, k, v, causal=True, scale=x.scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, dog, causal=True, scale=x.scale)
+    assert fa.debug_read_status() == 0
+    for b, h in ((0, 0), (2, 17), (3, 31)):
+        sl = lambda t: t[b:b + 1, :, h:h + 1]
+        rq, rk, rv = orc.attn_bwd(sl(x.q), sl(x.k), sl(x.v), sl(do), x.scale, True)
+        for name, a, r in (("dq", sl(dq), rq), ("dk", sl(dk), rk), ("dv", sl(dv), rv)):
+            mx, mean, rmax, rmean = _grad_err(a, r)
+            assert mx <= 2e-2 * max(1.0, rmax), f"{name} ({b},{h}): max err {mx:.3e} (ref max {rmax:.3f})"
+            assert mean <= 4e-3 * max(rmean, 1e-3), f"{name} ({b},{h}): mean err {mean:.3e}"
