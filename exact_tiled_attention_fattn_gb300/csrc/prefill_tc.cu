@@ -807,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = ex2(m - base);                        // 1 when m is kept
         const uint64_t nbase2 = f2_pack(-base, -base);
         const uint64_t mul2 = kMasked ? f2_pack(kLog2e, kLog2e) : sl2x2;
-        uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};  // row-sum partials, packed pairs
+        uint64_t acc2[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};  // row-sum partials, packed pairs
         // a column pair of P: bf16x2, or (FP8 variant) E4M3x2 in the low 16 bits
         auto pack_p = [](float p0, float p1) -> uint32_t {
           if constexpr (kFp8)
@@ -822,7 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float a0, a1;
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, nbase2), a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
-            acc2[(c >> 1) & 3] = f2_add(acc2[(c >> 1) & 3], f2_pack(p0, p1));
+            acc2[(c >> 1) & 7] = f2_add(acc2[(c >> 1) & 7], f2_pack(p0, p1));
             pk[c / 2] = pack_p(p0, p1);
           }
         } else {
@@ -832,10 +832,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             float a0, a1;
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
             const float p0 = c < vis ? ex2(a0) : 0.f, p1 = c + 1 < vis ? ex2(a1) : 0.f;
-            acc2[(c >> 1) & 3] = f2_add(acc2[(c >> 1) & 3], f2_pack(p0, p1));
+            acc2[(c >> 1) & 7] = f2_add(acc2[(c >> 1) & 7], f2_pack(p0, p1));
             pk[c / 2] = pack_p(p0, p1);
           }
         }
+        for (int i = 0; i < 4; ++i) acc2[i] = f2_add(acc2[i], acc2[i + 4]);
         float acc[8];
         f2_unpack(acc2[0], acc[0], acc[1]);
         f2_unpack(acc2[1], acc[2], acc[3]);
