@@ -725,11 +725,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile's 128 mask entries, requested before waiting for S (16-byte loads
         // of whole 8-key groups; groups at or past the visible limit are not read)
         uint4 mv[kMasked ? BN / 8 : 1];
-        if constexpr (kMasked) {
+        auto load_mask = [&](int c8) {
+          mv[c8] = j * BN + 8 * c8 < lim ? __ldg(reinterpret_cast<const uint4*>(mrow + j * BN + 8 * c8))
+                                         : make_uint4(0u, 0u, 0u, 0u);
+        };
+        if constexpr (kMasked) {  // the first half now, the second once S has arrived
 #pragma unroll
-          for (int c8 = 0; c8 < BN / 8; ++c8)
-            mv[c8] = j * BN + 8 * c8 < lim ? __ldg(reinterpret_cast<const uint4*>(mrow + j * BN + 8 * c8))
-                                           : make_uint4(0u, 0u, 0u, 0u);
+          for (int c8 = 0; c8 < BN / 16; ++c8) load_mask(c8);
         }
         if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status)) {
           ok = false;
@@ -745,6 +747,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           // exponent), one packed FMA per column pair, 32 columns at a time so each
           // mask word dies as its scores arrive; keys past the visible limit -inf
           // (their p is 0 below)
+#pragma unroll
+#pragma unroll
+          for (int c8 = BN / 16; c8 < BN / 8; ++c8) load_mask(c8);
 #pragma unroll
           for (int q32 = 0; q32 < BN / 32; ++q32) {
             uint32_t u[32];
@@ -807,6 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float alpha = ex2(m - base);                        // 1 when m is kept
         const uint64_t nbase2 = f2_pack(-base, -base);
         const uint64_t mul2 = kMasked ? f2_pack(kLog2e, kLog2e) : sl2x2;
+        constexpr int kAcc = kMasked ? 2 : 8;  // packed row-sum partials (fewer registers when masked)
         uint64_t acc2[8] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};  // row-sum partials, packed pairs
         // a column pair of P: bf16x2, or (FP8 variant) E4M3x2 in the low 16 bits
         auto pack_p = [](float p0, float p1) -> uint32_t {
@@ -822,7 +828,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float a0, a1;
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), mul2, nbase2), a0, a1);
             const float p0 = ex2(a0), p1 = ex2(a1);
-            acc2[(c >> 1) & 7] = f2_add(acc2[(c >> 1) & 7], f2_pack(p0, p1));
+            acc2[(c >> 1) & (kAcc - 1)] = f2_add(acc2[(c >> 1) & (kAcc - 1)], f2_pack(p0, p1));
             pk[c / 2] = pack_p(p0, p1);
           }
         } else {
@@ -832,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float a0, a1;
             f2_unpack(f2_fma(f2_pack(s[c], s[c + 1]), sl2x2, nbase2), a0, a1);
             const float p0 = c < vis ? ex2(a0) : 0.f, p1 = c + 1 < vis ? ex2(a1) : 0.f;
-            acc2[(c >> 1) & 7] = f2_add(acc2[(c >> 1) & 7], f2_pack(p0, p1));
+            acc2[(c >> 1) & (kAcc - 1)] = f2_add(acc2[(c >> 1) & (kAcc - 1)], f2_pack(p0, p1));
             pk[c / 2] = pack_p(p0, p1);
           }
         }
