@@ -360,10 +360,13 @@ def decode_workspace_size(B: int, Hq: int, d: int, num_splits: int) -> int:
 
 
 def choose_num_splits(batch: int, hkv: int, max_pages_per_seq: int, num_sms: int | None = None,
-                      chunk_pages: int = 128) -> int:
+                      chunk_pages: int = 256) -> int:
     """A split count that cuts contexts into ~``chunk_pages``-page chunks and gives at
     least two work items per SM over the batch. Larger chunks amortise each item's
-    fixed cost (Q load, pipeline fill, partial write); smaller ones balance better."""
+    fixed cost (Q load, pipeline fill, partial write); smaller ones balance better.
+    On the 8 x 64k-context decode workload, 256-page chunks (16 splits) read the KV
+    cache at 85.6 % of the measured HBM bandwidth against 81 % for 128-page chunks
+    (32 splits), 83 % for 12 splits and 63 % for 8."""
     if num_sms is None:
         num_sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     by_chunk = -(-max_pages_per_seq // chunk_pages)
