@@ -87,6 +87,20 @@ def recorded_traffic(kernel: str):
     return None
 
 
+def max_over_ranks(vals, world: int, device=None):
+    """Each value's maximum over the ranks (the slowest replica sets the step time).
+    One rank: the values unchanged. Works on any process group backend (NCCL on the
+    GPU machine with a CUDA device, gloo in the CPU tests with device=None)."""
+    vals = [float(v) for v in vals]
+    if world <= 1:
+        return vals
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu().tolist()]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -497,10 +511,7 @@ def main():
     dec_ms = [e[2].elapsed_time(e[3]) for e in ev]
     t_pre = sum(pre_ms) / len(pre_ms)
     t_dec = sum(dec_ms) / len(dec_ms)
-    if world > 1:
-        tt = torch.tensor([t_pre, t_dec], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_pre, t_dec = tt.tolist()
+    t_pre, t_dec = max_over_ranks([t_pre, t_dec], world, dev)
 
     flops = pre.flops()
     kv_bytes = dec.kv_bytes()
@@ -556,10 +567,7 @@ def main():
         torch.cuda.synchronize()
         tp = sum(e[0].elapsed_time(e[1]) for e in ee) / n_e2e
         td = sum(e[1].elapsed_time(e[2]) for e in ee) / n_e2e
-        if world > 1:
-            tt = torch.tensor([tp, td], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            tp, td = tt.tolist()
+        tp, td = max_over_ranks([tp, td], world, dev)
         e2e = {"value": world * flops / (tp * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d_pre + h2d_dec, "d2h_bytes_per_step": d2h_pre + d2h_dec,
                "prefill_ms": tp, "decode_ms": td,
