@@ -130,9 +130,10 @@ struct Item {
 };
 
 // Work-item order. Heads (b, h) are taken in groups whose items fill about four
-// rounds of the grid (measured against one, two, three, six, eight and sixteen:
-// four is within 1 % of the best on short causal sequences and 6 % faster than
-// two on 32k-token ones); inside a group the items go heaviest causal Q pair first
+// rounds of the grid when a head has at least 32 query-tile pairs, else two
+// (measured against one to sixteen rounds: four is 6 % faster than two on
+// 32k-token causal sequences, the same on 4k-token ones, and 20 % slower on the
+// short packed sequences of a varlen batch); inside a group the items go heaviest causal Q pair first
 // (all heads of the group at one pair index, then the next), and the grid walks
 // the item list in alternating direction round by round ("snake"), so each CTA
 // pairs heavy items with light ones while the K/V of the few heads in flight
@@ -146,7 +147,8 @@ __device__ __forceinline__ Schedule make_schedule(const PrefillParams& p) {
   s.pairs = (p.N + kRowsPerItem - 1) / kRowsPerItem;
   s.heads = p.B * p.Hq;
   const int G = p.Hq / p.Hkv;
-  int grp = (4 * (int)gridDim.x + s.pairs - 1) / s.pairs;   // heads per group
+  const int rounds = s.pairs >= 32 ? 4 : 2;                 // grid rounds per group
+  int grp = (rounds * (int)gridDim.x + s.pairs - 1) / s.pairs;  // heads per group
   grp = ((grp + G - 1) / G) * G;                            // whole GQA groups
   s.group = grp < s.heads ? grp : s.heads;
   s.total = s.heads * s.pairs;
