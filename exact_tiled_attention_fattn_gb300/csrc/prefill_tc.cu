@@ -59,18 +59,23 @@ constexpr int kRowsPerItem = 2 * BM;
 constexpr int kThreads = 384;    // 3 warpgroups
 // Register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded
 // down to the allocation granularity), i.e. 384 * 168 = 64512 in total. The
-// producer/MMA warpgroup drops to 88 and the two softmax warpgroups rise to 208:
-// 128 * 88 + 256 * 208 = 64512. The build checks that ptxas launches this
-// kernel at exactly kRegsLaunch registers.
+// producer/MMA warpgroup drops to 96 and the two softmax warpgroups rise to 200
+// (128 * 96 + 256 * 200 = 63488), the split at which no variant but the masked
+// one spills (88 / 208 left 16-byte spills in the control warps: 1-2 % slower).
+// The build checks that ptxas launches this kernel at exactly kRegsLaunch.
 constexpr int kRegsLaunch = 168;
-constexpr int kRegsControl = 88;
-constexpr int kRegsSoftmax = 208;
+constexpr int kRegsControl = 96;
+constexpr int kRegsSoftmax = 200;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 // The block-sparse variant's walks over the mask bits need more registers in
 // the producer/MMA/mask warpgroup: 128 * 104 + 256 * 200 = 64512.
 constexpr int kRegsControlSparse = 104;
 constexpr int kRegsSoftmaxSparse = 200;
 static_assert(128 * kRegsControlSparse + 256 * kRegsSoftmaxSparse <= kThreads * kRegsLaunch, "register split");
+// The masked variant holds mask entries in the softmax warps: 128 * 88 + 256 * 208 = 64512.
+constexpr int kRegsControlMasked = 88;
+constexpr int kRegsSoftmaxMasked = 208;
+static_assert(128 * kRegsControlMasked + 256 * kRegsSoftmaxMasked <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
@@ -299,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsControlSparse : kRegsControl));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsControlSparse : kMasked ? kRegsControlMasked : kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Lane 0 issues every copy; the paged variant runs lanes 0-7 through the same
@@ -661,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsSoftmaxSparse : kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsSoftmaxSparse : kMasked ? kRegsSoftmaxMasked : kRegsSoftmax));
     // ------------------------------------------------------------ softmax (tile t)
     const int t = (warp - 4) >> 2;           // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may touch
