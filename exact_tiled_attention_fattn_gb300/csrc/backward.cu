@@ -196,6 +196,16 @@ __device__ __forceinline__ void issue_tn(uint32_t d_tmem, uint32_t a_tmem, uint6
     mma_ts_acc(d_tmem, a_tmem + (ks >> 2) * 64 + (ks & 3) * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), id);
 }
 
+// The same product with A packed contiguously: keys 16 k live at columns [8 k, 8 k + 8).
+template <int D>
+__device__ __forceinline__ void issue_tn_packed(uint32_t d_tmem, uint32_t a_tmem, uint64_t b0, bool acc) {
+  constexpr uint32_t id = idesc_bf16_f32(BT, D, 1);
+  mma_ts(d_tmem, a_tmem, b0, id, acc ? 1u : 0u);
+#pragma unroll
+  for (int ks = 1; ks < BT / 16; ++ks)
+    mma_ts_acc(d_tmem, a_tmem + ks * 8, b0 + (uint64_t)(ks * 16 * 128 / 16), id);
+}
+
 // Load 128-row tile (rows r0.., head h) of a [rows, H, D] tensor map into dst.
 template <int D>
 __device__ __forceinline__ void load_tile(uint32_t dst, const CUtensorMap* map, uint32_t bar, int h, int r0,
@@ -530,11 +540,13 @@ struct DqLayout {
   static constexpr int kTile = BwdTiles<D>::kTile;
   static constexpr int kOffQ = 0;
   static constexpr int kOffDO = kTile;
-  static constexpr int kOffRing = 2 * kTile;      // stage s: K_j, V_j
-  static constexpr int kStage = 2 * kTile;
-  static constexpr int kStages = 2;
-  static constexpr int kOffBar = kOffRing + kStages * kStage;
-  static constexpr int kNumBars = 14;
+  // K_j lives in stage j % 3 of the K ring (read by S_j and dQ += dS_j K_j), V_j in
+  // stage j % 2 of the V ring (read by dP_j alone, so it is released two products sooner)
+  static constexpr int kKStages = 3, kVStages = 2;
+  static constexpr int kOffK = 2 * kTile;
+  static constexpr int kOffV = kOffK + kKStages * kTile;
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
+  static constexpr int kNumBars = 20;
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
@@ -544,9 +556,13 @@ struct DqLayout {
   static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 enum : int {
-  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 4, kQSFull = 6, kQSFree = 7, kQDpFull = 8, kQDsFull = 9,
-  kQAccFull = 10, kQAccEmpty = 11, kQMmaDone = 12
+  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 5, kVFull = 8, kVEmpty = 10, kQSFull = 12, kQSFree = 13,
+  kQDpFull = 14, kQDpFree = 15, kQDsFull = 16, kQAccFull = 17, kQAccEmpty = 18, kQMmaDone = 19
 };
+// dQ pass: dS of key tile n goes to TMEM columns [kColDs + 64 (n & 1), +64) (bf16 pairs;
+// warpgroup g writes the 32 columns of its keys at + 32 g), so dP of the next tile can be
+// written while dS of this one still feeds dQ += dS K.
+constexpr uint32_t kColDs = 384;
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -563,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kQSFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
+      mbar_init(bar(i), (i == kQSFree || i == kQDpFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -597,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      uint32_t nq = 0, nkv = 0;
+      uint32_t nq = 0, nk = 0, nv = 0;
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
       bool ok = true;
       for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
@@ -610,35 +626,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
         const int jn = p.causal ? i + 1 : nt, hkv = h / G;
         for (int j = 0; j < jn; ++j) {
-          const uint32_t st = nkv & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
-          if (!mbar_wait(bar(kKEmpty + st), ((nkv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          const uint32_t ks = nk % 3, vs = nv & 1;
+          if (!mbar_wait(bar(kKEmpty + ks), ((nk / 3) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kKFull + st), 2 * Lay::kTile);
-          load_tile<D>(base, &tk, bar(kKFull + st), hkv, b * p.N + j * BT, pol_kv);
-          load_tile<D>(base + Lay::kTile, &tv, bar(kKFull + st), hkv, b * p.N + j * BT, pol_kv);
-          ++nkv;
+          mbar_arrive_expect_tx(bar(kKFull + ks), Lay::kTile);
+          load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kKFull + ks), hkv, b * p.N + j * BT, pol_kv);
+          ++nk;
+          if (!mbar_wait(bar(kVEmpty + vs), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(kVFull + vs), Lay::kTile);
+          load_tile<D>(sb + Lay::kOffV + vs * Lay::kTile, &tv, bar(kVFull + vs), hkv, b * p.N + j * BT, pol_kv);
+          ++nv;
         }
       }
+      // wait for the last load into each buffer before the CTA may exit
       if (nq) mbar_drain(bar(kQFull), (nq - 1) & 1);
-      for (uint32_t st = 0; st < 2; ++st) {
-        const uint32_t c = (nkv + 1 - st) / 2;
+      for (uint32_t st = 0; st < 3; ++st) {
+        const uint32_t c = (nk + 2 - st) / 3;
         if (c) mbar_drain(bar(kKFull + st), (c - 1) & 1);
+      }
+      for (uint32_t st = 0; st < 2; ++st) {
+        const uint32_t c = (nv + 1 - st) / 2;
+        if (c) mbar_drain(bar(kVFull + st), (c - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // per key tile j: S_j = Q K_j^T, dP_j = dO V_j^T, then (once the element-wise
-    // warps have read S_j) S_{j+1}, then dQ += dS_j K_j.
+    // per key tile j: S_j = Q K_j^T and dP_j = dO V_j^T; S_{j+1} as soon as the
+    // element-wise warps have read S_j, dP_{j+1} as soon as they have read dP_j,
+    // then dQ += dS_j K_j once dS_j is written. dS alternates between two TMEM
+    // buffers: dS_{n+2} is written only after dP_{n+2} completes, which was issued
+    // after dQ += dS_n K_n, so that product has finished reading buffer n & 1.
     if (lane == 0) {
-      uint32_t nq = 0, nkv = 0, nfree = 0, nds = 0, nacc = 0;
+      // n counts key tiles over all items: K_n in K stage n % 3, V_n in V stage n % 2
+      uint32_t nq = 0, n = 0, nfree = 0, ndpf = 0, nacc = 0;
       const uint64_t qd = smem_desc_sw128(sb + Lay::kOffQ, 16, 1024);
       const uint64_t dod = smem_desc_sw128(sb + Lay::kOffDO, 16, 1024);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColAcc;
       bool ok = true;
-      auto wait_kv = [&](uint32_t n) -> bool {
-        return mbar_wait(bar(kKFull + (n & 1)), (n >> 1) & 1, abort, p.status, kWaitLimitNs);
+      auto k_addr = [&](uint32_t t) -> uint32_t { return sb + Lay::kOffK + (t % 3) * Lay::kTile; };
+      auto v_addr = [&](uint32_t t) -> uint32_t { return sb + Lay::kOffV + (t & 1) * Lay::kTile; };
+      // S_t = Q K_t^T
+      auto issue_s = [&](uint32_t t) -> bool {
+        if (!mbar_wait(bar(kKFull + t % 3), (t / 3) & 1, abort, p.status, kWaitLimitNs)) return false;
+        tc_fence_after();
+        issue_kk<D>(tS, qd, smem_desc_sw128(k_addr(t), 16, 1024));
+        mma_commit(bar(kQSFull));
+        return true;
+      };
+      // dP_t = dO V_t^T, then V_t's stage is free
+      auto issue_dp = [&](uint32_t t) -> bool {
+        if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1, abort, p.status, kWaitLimitNs)) return false;
+        tc_fence_after();
+        issue_kk<D>(tDP, dod, smem_desc_sw128(v_addr(t), 16, 1024));
+        mma_commit(bar(kQDpFull));
+        mma_commit(bar(kVEmpty + (t & 1)));
+        return true;
       };
       for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, h, i;
@@ -646,42 +693,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jn = p.causal ? i + 1 : nt;
         if (!mbar_wait(bar(kQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
         ++nq;
-        if (!wait_kv(nkv)) break;
-        tc_fence_after();
-        issue_kk<D>(tS, qd, smem_desc_sw128(sb + Lay::kOffRing + (nkv & 1) * Lay::kStage, 16, 1024));
-        mma_commit(bar(kQSFull));
-        for (int j = 0; j < jn; ++j) {
-          const uint32_t st = nkv & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
-          issue_kk<D>(tDP, dod, smem_desc_sw128(base + Lay::kTile, 16, 1024));  // dP = dO V_j^T
-          mma_commit(bar(kQDpFull));
+        if (!issue_s(n) || !issue_dp(n)) break;
+        for (int j = 0; j < jn; ++j, ++n) {
           if (j + 1 < jn) {
-            if (!wait_kv(nkv + 1) || !mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs)) {
+            if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs) || !issue_s(n + 1)) {
               ok = false;
               break;
             }
             ++nfree;
-            tc_fence_after();
-            issue_kk<D>(tS, qd, smem_desc_sw128(sb + Lay::kOffRing + ((nkv + 1) & 1) * Lay::kStage, 16, 1024));
-            mma_commit(bar(kQSFull));
+            if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, kWaitLimitNs) || !issue_dp(n + 1)) {
+              ok = false;
+              break;
+            }
+            ++ndpf;
           }
           if (j == 0 && !mbar_wait(bar(kQAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(bar(kQDsFull), nds & 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kQDsFull), n & 1, abort, p.status, kWaitLimitNs)) {
             ok = false;
             break;
           }
-          ++nds;
           tc_fence_after();
-          issue_tn<D>(tDQ, tDP, smem_desc_sw128(base, BT * 128, 1024), j > 0);  // dQ += dS K_j
-          mma_commit(bar(kKEmpty + st));
-          ++nkv;
+          issue_tn_packed<D>(tDQ, tmem + kColDs + 64 * (n & 1), smem_desc_sw128(k_addr(n), BT * 128, 1024), j > 0);
+          mma_commit(bar(kKEmpty + n % 3));  // dQ += dS_n K_n
         }
         if (!ok) break;
-        // the last S of the item was read before its dS was written
-        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs)) break;
+        // the item's last S and dP were read before its last dS was written
+        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs) ||
+            !mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, kWaitLimitNs))
+          break;
         ++nfree;
+        ++ndpf;
         mma_commit(bar(kQEmpty));
         mma_commit(bar(kQAccFull));
         ++nacc;
@@ -696,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = 64 * wg;                          // this warpgroup's key columns
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_col = tmem + lane_off + kColS + cb, dp_col = tmem + lane_off + kColDP + cb;
-    const uint32_t dq_col = tmem + lane_off + kColAcc;
+    const uint32_t dq_col = tmem + lane_off + kColAcc, ds_col = tmem + lane_off + kColDs + 32 * wg;
     const float sl2 = p.scale * kLog2e;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t ns = 0, ndp = 0, nacc = 0;
@@ -737,9 +781,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        ++ndp;
         tc_fence_after();
-        write_ds<false>(dp_col, pv, nullptr, dval);
+        {
+          uint32_t a[64];
+          tmem_ld64(dp_col, a);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(kQDpFree));  // dP may be overwritten by the next tile's product
+          // dS = P o (dP - D) as bf16 pairs
+          uint32_t w[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            w[e] = pack_bf16x2(pv[2 * e] * (__uint_as_float(a[2 * e]) - dval),
+                               pv[2 * e + 1] * (__uint_as_float(a[2 * e + 1]) - dval));
+          tmem_st32(ds_col + 64 * (ndp & 1), w);
+        }
+        ++ndp;
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
