@@ -67,8 +67,9 @@ constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 96;
 constexpr int kRegsSoftmax = 200;
 static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
-// The block-sparse variant's walks over the mask bits need more registers in
-// the producer/MMA/mask warpgroup: 128 * 104 + 256 * 200 = 64512.
+// The block-sparse variant's walks over the mask bits, and the dense d = 64
+// variant's separate S and P schedule, need more registers in the
+// producer/MMA(/mask) warpgroup: 128 * 104 + 256 * 200 = 64512.
 constexpr int kRegsControlSparse = 104;
 constexpr int kRegsSoftmaxSparse = 200;
 static_assert(128 * kRegsControlSparse + 256 * kRegsSoftmaxSparse <= kThreads * kRegsLaunch, "register split");
@@ -92,8 +93,26 @@ constexpr int kMaskSlotBytes = 2 * kMaskWords * 4 + 16;
 constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8 softmax warps
 static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
-template <int D, bool kFp8 = false>
+// barrier slots
+enum : int {
+  kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8,
+  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16,
+  kBarMaskFull = 17, kBarMaskEmpty = 17 + kMaskSlots,
+  // separate P buffers (dense d = 64): S_t read by the softmax, O_t += P_t V completed
+  kBarSFree = 17 + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
+};
+
+enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
+
+template <int D, int kMode>
 struct TcLayout {
+  static constexpr bool kFp8 = kMode == kModeFp8;
+  // S_t(j + 1) issued as soon as the softmax has read S_t(j), not after P_t(j) V, where P
+  // does not overwrite S: the dense variant at d = 64 (S_A, S_B, O_A and O_B take 384 TMEM
+  // columns, so P_A and P_B get buffers of their own in the other 128, bf16 pairs, 64
+  // columns each) and the FP8 variant (P in shared memory).
+  static constexpr bool kPTmem = kMode == kModeDense && D == 64;
+  static constexpr bool kEarly = kPTmem || kFp8;
   static constexpr int kElem = kFp8 ? 1 : 2;      // bytes per Q/K/V element (E4M3 or bf16)
   static constexpr int kQBytes = BM * D * kElem;  // one Q tile
   static constexpr int kKVBytes = BN * D * kElem;
@@ -102,7 +121,7 @@ struct TcLayout {
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kStages * kKVBytes;
-  static constexpr int kNumBars = 17 + 2 * kMaskSlots;
+  static constexpr int kNumBars = kEarly ? kBarCount : kBarSFree;
   static constexpr int kOffHolder = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffMask = kOffAbort + 8;  // block-mask ring (block-sparse variant)
@@ -117,14 +136,9 @@ struct TcLayout {
   // columns), fp32 O_A, O_B.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
   __host__ __device__ static constexpr uint32_t col_o(int t) { return t ? 256u + D : 256u; }
+  __host__ __device__ static constexpr uint32_t col_p(int t) { return t ? 448u : 384u; }  // kPTmem only
   static_assert(256 + 2 * D <= kTmemCols, "TMEM budget");
-};
-
-// barrier slots
-enum : int {
-  kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8,
-  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16,
-  kBarMaskFull = 17, kBarMaskEmpty = 17 + kMaskSlots
+  static_assert(!kPTmem || 256 + 2 * D <= 384, "TMEM budget with P buffers");
 };
 
 struct Item {
@@ -254,7 +268,6 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // Variants of the kernel (template argument kMode).
-enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
 
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -266,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V^T; P in E4M3 through shared memory
   static_assert(!kFp8 || D == 128, "FP8 tiles are 128 one-byte columns: one 128-byte swizzle span");
   constexpr int kChunks = kFp8 ? 1 : D / 64;      // 128-byte boxes per tile row
-  using Lay = TcLayout<D, kFp8>;
+  using Lay = TcLayout<D, kMode>;
+  constexpr bool kEarly = Lay::kEarly;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -280,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1) ? 4
-                        : (i >= kBarMaskEmpty)                  ? kMaskConsumers
-                                                                : 1);
+      mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1 || i == kBarSFree || i == kBarSFree + 1) ? 4
+                        : (i >= kBarMaskEmpty && i < kBarMaskEmpty + kMaskSlots)                ? kMaskConsumers
+                                                                                                 : 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsControlSparse : kMasked ? kRegsControlMasked : kRegsControl));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsControlSparse : kMasked ? kRegsControlMasked : kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Lane 0 issues every copy; the paged variant runs lanes 0-7 through the same
@@ -432,6 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);   // P V: V is MN-major (d contiguous)
       uint32_t nq = 0, nk = 0, nv = 0;
       uint32_t np[2] = {0, 0};                             // P_X buffers consumed so far
+      uint32_t si[2] = {0, 0};                             // S_X issued (dense d = 64)
       // Descriptor bases, built once. The start-address field (bits 0-13, in
       // 16-byte units) of each per-MMA descriptor is the base plus a
       // compile-time offset, so issuing an MMA costs no descriptor arithmetic.
@@ -466,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarPFull + t), np[t] & 1, abort, p.status, kWaitLimitNs)) return false;
         ++np[t];
         tc_fence_after();
-        const uint32_t p_tmem = tmem + Lay::col_s(t), o_tmem = tmem + Lay::col_o(t);
+        const uint32_t p_tmem = tmem + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t)), o_tmem = tmem + Lay::col_o(t);
         const uint64_t b0 = vst ? vd1 : vd0;
         if constexpr (kFp8) {  // O += P V with P (E4M3, shared memory) and V^T both K-major
           constexpr uint32_t idO8 = idesc_e4m3_f32(BM, D);
@@ -562,6 +577,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
         ++nq;
         tc_fence_after();
+        if constexpr (kEarly) {
+          // per K/V tile j: S_A(j) and S_B(j) once each softmax has read its previous S,
+          // then O_t += P_t(j-1) V_{j-1} once P_t(j-1) is written
+          auto early_s = [&](int t, uint32_t kst) -> bool {
+            if (si[t] > 0 && !mbar_wait(bar(kBarSFree + t), (si[t] - 1) & 1, abort, p.status, kWaitLimitNs))
+              return false;
+            ++si[t];
+            tc_fence_after();
+            issue_s(t, kst);
+            return true;
+          };
+          auto early_pv = [&](int t, uint32_t vst, bool acc) -> bool {
+            if (!issue_pv(t, vst, acc)) return false;
+            mma_commit(bar(kBarPvDone + t));  // P_t's buffer is free and O_t holds the tile
+            return true;
+          };
+          for (int j = 0; ok && j <= n; ++j) {
+            if (j < n) {
+              const uint32_t kst = nk & 1;
+              if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
+                  (j < nA && !early_s(0, kst)) || (j < nB && !early_s(1, kst))) {
+                ok = false;
+                break;
+              }
+              mma_commit(bar(kBarKEmpty + kst));
+              ++nk;
+              if (j == n - 1) mma_commit(bar(kBarQEmpty));
+            }
+            if (j > 0) {
+              const uint32_t vst = nv & 1;
+              if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              if ((j - 1 < nA && !early_pv(0, vst, j - 1 > 0)) || (j - 1 < nB && !early_pv(1, vst, j - 1 > 0))) {
+                ok = false;
+                break;
+              }
+              mma_commit(bar(kBarVEmpty + vst));
+              ++nv;
+            }
+          }
+          continue;
+        }
         // j = 0
         {
           const uint32_t kst = nk & 1;
@@ -666,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSparse ? kRegsSoftmaxSparse : kMasked ? kRegsSoftmaxMasked : kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsSoftmaxSparse : kMasked ? kRegsSoftmaxMasked : kRegsSoftmax));
     // ------------------------------------------------------------ softmax (tile t)
     const int t = (warp - 4) >> 2;           // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may touch
@@ -679,6 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     const uint64_t scale2 = f2_pack(p.scale, p.scale);
     uint32_t ns = 0, no = 0;                 // S_t and O_t completions seen
+    uint32_t npv = 0;                        // O_t += P_t V completions seen (dense d = 64)
+    const uint32_t p_col = tmem + lane_off + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t));
     uint32_t nm = 0;                         // block-mask slots consumed
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -788,6 +850,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int e = 0; e < BN; ++e) s[e] = __uint_as_float(u[e]);
           }
+          if constexpr (kEarly) {  // S_t(j) is in registers: the next product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + t));
+          }
         }
         if (!kMasked && masked) {
 #pragma unroll
@@ -859,6 +926,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(acc2[3], acc[6], acc[7]);
         const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * alpha + sum;
+        if constexpr (kEarly) {
+          // O_t += P_t(j-1) V has completed: O_t may be rescaled and P_t's buffer rewritten
+          if (!first) {
+            if (!warp_wait(bar(kBarPvDone + t), npv & 1, abort, p.status)) {
+              ok = false;
+              break;
+            }
+            ++npv;
+            tc_fence_after();
+          }
+        }
         if (!first && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O_t += P_t(j-1) V has completed (covered by the commit of S_t(j)).
 #pragma unroll
@@ -876,7 +954,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // P in E4M3 (p <= 2^8 < 448, the largest finite value), row r of the tile's
           // 128 x 128-byte buffer, 16-byte chunk c at chunk position c ^ (r mod 8) (the
           // 128-byte swizzle the descriptor declares). P_t's previous product has
-          // completed: it was issued before S_t(j), whose completion this thread saw.
+          // completed (the wait above).
           uint8_t* prow = smem + Lay::kOffP + t * Lay::kPBytes + r * 128;
 #pragma unroll
           for (int c16 = 0; c16 < 8; ++c16) {
@@ -888,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           fence_proxy_async_smem();
         } else {
-          tmem_st64(s_col, pk);
+          tmem_st64(p_col, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -898,11 +976,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       release_mask();
       // epilogue: O / l in bf16 and the row's logsumexp
-      if (!warp_wait(bar(kBarOFull + t), no & 1, abort, p.status)) {
+      if (!warp_wait(bar(kEarly ? kBarPvDone + t : kBarOFull + t), (kEarly ? npv : no) & 1, abort, p.status)) {
         ok = false;
         break;
       }
-      ++no;
+      if (kEarly)
+        ++npv;
+      else
+        ++no;
       tc_fence_after();
       const bool live = row < x.L;
       // a row the mask left with no key: O = 0, lse = -inf
@@ -943,7 +1024,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                      int num_sms, cudaStream_t stream) {
-  using Lay = TcLayout<D, kMode == kModeFp8>;
+  using Lay = TcLayout<D, kMode>;
   auto kern = prefill_tc_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
   if (e != cudaSuccess) return e;
