@@ -108,10 +108,10 @@ template <int D, int kMode>
 struct TcLayout {
   static constexpr bool kFp8 = kMode == kModeFp8;
   // S_t(j + 1) issued as soon as the softmax has read S_t(j), not after P_t(j) V, where P
-  // does not overwrite S: the dense variant at d = 64 (S_A, S_B, O_A and O_B take 384 TMEM
+  // does not overwrite S: the dense, paged and masked variants at d = 64 (S_A, S_B, O_A and O_B take 384 TMEM
   // columns, so P_A and P_B get buffers of their own in the other 128, bf16 pairs, 64
   // columns each) and the FP8 variant (P in shared memory).
-  static constexpr bool kPTmem = kMode == kModeDense && D == 64;
+  static constexpr bool kPTmem = (kMode == kModeDense || kMode == kModePaged || kMode == kModeMasked) && D == 64;
   static constexpr bool kEarly = kPTmem || kFp8;
   static constexpr int kElem = kFp8 ? 1 : 2;      // bytes per Q/K/V element (E4M3 or bf16)
   static constexpr int kQBytes = BM * D * kElem;  // one Q tile
@@ -836,6 +836,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               s[c] = t0;
               s[c + 1] = t1;
             }
+          }
+          if constexpr (kEarly) {  // S_t(j) is in registers: the next product may overwrite it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(kBarSFree + t));
           }
           if (masked) {
 #pragma unroll
