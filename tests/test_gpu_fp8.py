@@ -53,3 +53,23 @@ def test_fp8_large_sampled(fa):
                                       rows=smp)
     bi, hi, ii = (torch.as_tensor(smp[:, c], device="cuda") for c in range(3))
     _check_fp8(o[bi, ii, hi], lse[bi, hi, ii], o_ref, lse_ref, "fp8 large")
+
+
+def test_fp8_lazy_rescale_after_mass_jumps(fa):
+    """E4M3 q = e_0, k[..., 0] = 6 per jump (tiles 3 and 7 of head 0, 1 and 5 of head 1;
+    6 and 12 are exact in E4M3), scale 1: the running max rises by 8.7 > 8 in log2 units
+    twice while the earlier tiles keep weight; V = (tile index + 1) / 8 + 0.02 N(0, 1), quantized."""
+    N, H, d = 1024, 2, 128
+    g = torch.Generator().manual_seed(43)
+    tile = torch.arange(N) // 128
+    q = torch.zeros(1, N, H, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, N, H, d)
+    for h, js in enumerate([(3, 7), (1, 5)]):
+        k[0, :, h, 0] = 6.0 * sum((tile >= t).float() for t in js)
+    v = (tile[None, :, None, None].float() + 1.0) / 8 + 0.02 * torch.randn(1, N, H, d, generator=g)
+    q8, k8, v8 = (t.to(torch.float8_e4m3fn).view(torch.uint8) for t in (q, k, v))
+    o, lse = fa.fwd_fp8(q8.cuda(), k8.cuda(), v8.cuda(), 1.0, 1.0, 1.0, causal=True, scale=1.0)
+    assert fa.debug_read_status() == 0
+    o_ref, lse_ref = orc.attn_fwd_fp8(q8, k8, v8, 1.0, 1.0, 1.0, 1.0, True)
+    _check_fp8(o, lse, o_ref, lse_ref, "fp8 rescale jumps")

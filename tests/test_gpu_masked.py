@@ -75,3 +75,21 @@ def test_alibi_bias_large_sampled(fa):
     o_ref, lse_ref = orc.attn_fwd_masked(x.q, x.k, x.v, x.scale, True, m.float().numpy(), rows=smp)
     bi, hi, ii = (torch.as_tensor(smp[:, c], device="cuda") for c in range(3))
     check(o[bi, ii, hi], lse[bi, hi, ii], o_ref, lse_ref, what="ALiBi-style bias")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_lazy_rescale_from_mask_jumps(fa, d):
+    """The mask raises whole key tiles (3 and 7) by 5.75 above the tiles before them
+    (q, k random, so the scores stay within a few units): the running max jumps by more
+    than 2^8 twice and O is rescaled while the earlier tiles still carry weight; V grows
+    with the tile index."""
+    N = 1024
+    x = inputs.prefill_dense(5400 + d, 1, N, 2, 2, d, False)
+    tile = torch.arange(N) // 128
+    col = 5.75 * ((tile >= 3).float() + (tile >= 7).float())
+    m = col[None, :].expand(N, N).to(torch.bfloat16)[None, None].contiguous()
+    v = ((tile[None, :, None, None].float() + 1.0) / 8 + 0.1 * x.v.float()).to(torch.bfloat16)
+    o, lse = fa.fwd_masked(x.q.cuda(), x.k.cuda(), v.cuda(), m.cuda(), causal=True, scale=x.scale)
+    assert fa.debug_read_status() == 0
+    o_ref, lse_ref = orc.attn_fwd_masked(x.q, x.k, v, x.scale, True, m.float().numpy())
+    check(o, lse, o_ref, lse_ref, what=f"mask jumps d={d}")

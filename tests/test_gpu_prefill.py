@@ -237,3 +237,34 @@ def test_causal_mha_config_sampled(fa):
 def test_long_gqa_config_sampled(fa):
     """B=1, Hq=32, Hkv=8, N=32768, d=128, causal, seed 2."""
     _sampled_check(fa, inputs.long_gqa_config(), "long GQA config")
+
+
+def _jump_inputs(N, H, d, jumps, step, seed):
+    """q = e_0 (scale 1), so a key's score is its k[..., 0]: every key of tile t of head h
+    scores `step` times the number of head h's jump tiles <= t. V of a key = (its tile
+    index + 1) / 8 plus 0.02 N(0, 1) noise (|O| <= 1, where the bf16 tolerances hold)."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.zeros(1, N, H, d)
+    q[..., 0] = 1.0
+    k = torch.zeros(1, N, H, d)
+    tile = torch.arange(N) // 128
+    for h, js in enumerate(jumps):
+        k[0, :, h, 0] = step * sum((tile >= t).float() for t in js)
+    v = (tile[None, :, None, None].float() + 1.0) / 8 + 0.02 * torch.randn(1, N, H, d, generator=g)
+    return q, k, v
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_lazy_rescale_after_mass_jumps(fa, d, causal):
+    """Whole key tiles (3 and 7 for head 0, 1 and 5 for head 1) score 5.75 above the tiles
+    before them: the running max rises by 8.3 > 8 in log2 units twice, so O is rescaled
+    while the earlier tiles still hold about 1 % of the weight, and V grows with the tile
+    index. A rescale that missed or double-counted one P V product (one still in flight
+    when O is scaled) moves O by about 0.8."""
+    q, k, v = _jump_inputs(1024, 2, d, [(3, 7), (1, 5)], 5.75, 41)
+    qb, kb, vb = q.bfloat16(), k.bfloat16(), v.bfloat16()
+    o, lse = fa.fwd(qb.cuda(), kb.cuda(), vb.cuda(), causal=causal, scale=1.0)
+    assert fa.debug_read_status() == 0
+    o_ref, lse_ref = orc.attn_fwd(qb, kb, vb, 1.0, causal)
+    check(o, lse, o_ref, lse_ref, what=f"rescale d={d} causal={causal}")
