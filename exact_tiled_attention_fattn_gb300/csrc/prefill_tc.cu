@@ -37,6 +37,11 @@
 // the product has read P_X(j-1) before S_X(j) overwrites those columns. The
 // softmax writes P_X(j) only after S_X(j) completed, whose commit covers every
 // earlier MMA, O_X += P_X(j-1) V included.
+// Where P_X has a buffer of its own (bf16 at d = 64: TMEM columns 384 and 448;
+// the FP8 variant: shared memory), S_X(j) is issued as soon as the softmax has
+// read S_X(j-1) into registers (barrier SFree), and the softmax waits for
+// O_X += P_X(j-1) V to complete (barrier PvDone, one commit per product) before
+// it rescales O_X or rewrites P_X; the epilogue waits for the last one.
 //
 // Every pipeline wait is bounded: a wait that exceeds its limit records
 // FATTN_ERR_TIMEOUT in the device status word, every role stops, in-flight
