@@ -396,18 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kKvFull), nkv & 1, abort, p.status, kWaitLimitNs)) break;
         ++nkv;
         tc_fence_after();
+        bool s_issued = false;  // S^T of step t already issued (early, in step t - 1)
         for (int t = 0; t < steps; ++t) {
           const uint32_t st = nqd & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
-          if (!mbar_wait(bar(kQdFull + st), (nqd >> 1) & 1, abort, p.status, kWaitLimitNs)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t qk = smem_desc_sw128(base, 16, 1024), dok = smem_desc_sw128(base + Lay::kTile, 16, 1024);
+          const uint64_t dok = smem_desc_sw128(base + Lay::kTile, 16, 1024);
           const uint64_t qmn = smem_desc_sw128(base, BT * 128, 1024);
           const uint64_t domn = smem_desc_sw128(base + Lay::kTile, BT * 128, 1024);
-          issue_kk<D>(tS, kd, qk);   // S^T = K Q^T (P^T of the previous step was read by its dV product)
-          mma_commit(bar(kSFull));
+          if (!s_issued) {
+            if (!mbar_wait(bar(kQdFull + st), (nqd >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_kk<D>(tS, kd, smem_desc_sw128(base, 16, 1024));  // S^T = K Q^T
+            mma_commit(bar(kSFull));
+          }
           issue_kk<D>(tDP, vd, dok);  // dP^T = V dO^T (dS^T of the previous step was read by its dK product)
           mma_commit(bar(kDpFull));
           if (t == 0 && !mbar_wait(bar(kAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
@@ -421,6 +424,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++np;
           tc_fence_after();
           issue_tn<D>(tDV, tS, domn, t > 0);  // dV += P^T dO
+          // The next S^T may follow right away if its Q stage has landed: it overwrites
+          // P^T, which only the dV product just issued reads (the element-wise warps keep
+          // P^T in registers for dS^T), and runs while they compute dS^T. Otherwise it
+          // waits until after dK, as the stage may still be loading.
+          s_issued = false;
+          if (t + 1 < steps) {
+            const uint32_t n1 = nqd + 1;
+            if (mbar_try_wait(bar(kQdFull + (n1 & 1)), (n1 >> 1) & 1)) {
+              tc_fence_after();
+              issue_kk<D>(tS, kd, smem_desc_sw128(sb + Lay::kOffRing + (n1 & 1) * Lay::kStage, 16, 1024));
+              mma_commit(bar(kSFull));
+              s_issued = true;
+            }
+          }
           if (!mbar_wait(bar(kDsFull), nds & 1, abort, p.status, kWaitLimitNs)) {
             ok = false;
             break;
