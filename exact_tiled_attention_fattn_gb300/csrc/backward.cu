@@ -16,20 +16,23 @@
 //                          accumulates dV and dK in TMEM:
 //                            S^T = K Q_i^T, dP^T = V dO_i^T (TMEM, fp32),
 //                            P^T (bf16, over S^T), dV += P^T dO_i,
-//                            dS^T (bf16, over dP^T), dK += dS^T Q_i.
+//                            dS^T (bf16, over dP^T), dK += dS^T Q_i;
+//                          the next S^T follows dV when its Q/dO stage has
+//                          landed (it overwrites only P^T, which dV reads).
 //   bwd_dq_kernel<d>       items (sequence, query head, 128-query tile i); an
 //                          item walks the key tiles j (causal: j <= i):
-//                            S = Q K_j^T, dP = dO V_j^T, dS (bf16, over dP),
-//                            dQ += dS K_j.
+//                            S = Q K_j^T, dP = dO V_j^T, dS (bf16, in two
+//                            TMEM buffers of its own), dQ += dS K_j.
 // dQ is computed in its own pass (recomputing S and dP) instead of being
 // accumulated with atomics from the dK/dV pass: at d = 128 the dK/dV pass
 // already uses all 512 TMEM columns (S^T, dP^T, dV, dK).
 //
 // Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread),
 // warps 4-7 and 8-11 the element-wise work: a thread owns one TMEM lane (tile
-// row), warpgroup g columns [64 g, 64 g + 64) of it. Each warpgroup packs its
-// bf16 P or dS into the first 32 columns of its own 64, so the two never touch
-// each other's columns and the MMA reads its TMEM operand from the two halves.
+// row), warpgroup g columns [64 g, 64 g + 64) of it. In the dK/dV pass each
+// warpgroup packs its bf16 P^T or dS^T into the first 32 columns of its own 64,
+// so the two never touch each other's columns and the MMA reads its TMEM
+// operand from the two halves; the dQ pass writes dS to columns 384-511.
 // Every pipeline wait is bounded as in the forward kernel: a wait past its
 // limit records FATTN_ERR_TIMEOUT, every role stops, copies and MMAs are
 // drained and TMEM is freed.
