@@ -88,6 +88,8 @@ def _check(fn: str, status: int):
 def _stream_handle(stream) -> int:
     if stream is None:
         stream = torch.cuda.current_stream()
+    elif stream.device.index != torch.cuda.current_device():
+        raise ValueError(f"stream is on {stream.device} but the current CUDA device is cuda:{torch.cuda.current_device()}")
     return int(stream.cuda_stream)
 
 
@@ -104,11 +106,24 @@ def _dtype_code(dt) -> int:
 
 
 def _need_cuda(*ts):
+    """All given tensors are contiguous CUDA tensors on one device, the current one
+    (the library launches on the current device, so a tensor elsewhere would be an
+    invalid address there)."""
+    dev = None
     for t in ts:
-        if t is not None and not t.is_cuda:
+        if t is None:
+            continue
+        if not t.is_cuda:
             raise ValueError("all tensors must be CUDA tensors")
-        if t is not None and not t.is_contiguous():
+        if not t.is_contiguous():
             raise ValueError("all tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"all tensors must be on one device (got {dev} and {t.device})")
+    if dev is not None and dev.index != torch.cuda.current_device():
+        raise ValueError(f"tensors are on {dev} but the current CUDA device is cuda:{torch.cuda.current_device()}; "
+                         f"call under torch.cuda.device({dev.index})")
 
 
 def _expect(t, shape, name, dtype=None):

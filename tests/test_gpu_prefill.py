@@ -268,3 +268,18 @@ def test_lazy_rescale_after_mass_jumps(fa, d, causal):
     assert fa.debug_read_status() == 0
     o_ref, lse_ref = orc.attn_fwd(qb, kb, vb, 1.0, causal)
     check(o, lse, o_ref, lse_ref, what=f"rescale d={d} causal={causal}")
+
+
+def test_binding_rejects_tensors_off_the_current_device(fa):
+    """The library launches on the current device: tensors (or a stream) on another
+    device are refused before any launch, as are tensors split across devices."""
+    if torch.cuda.device_count() < 2:
+        pytest.skip("needs two GPUs")
+    q = torch.zeros(1, 128, 1, 64, dtype=torch.bfloat16, device="cuda:1")
+    with pytest.raises(ValueError):
+        fa.fwd(q, q, q)
+    with pytest.raises(ValueError):
+        fa.fwd(q.to("cuda:0"), q, q)
+    with torch.cuda.device(1):
+        o, _ = fa.fwd(q, q, q)
+        assert o.device == q.device
