@@ -6,8 +6,9 @@
 // long K/V. A persistent grid takes work items (sequence, KV head, split) from
 // a counter in the workspace, highest split first; an item covers all query
 // heads of that KV head's GQA group (up to 16), so each K/V byte is read once,
-// and an empty split costs one atomic instead of a thread block. Each of the 4 warps streams its own 16-token chunks through a 3-stage
-// cp.async pipeline (16-byte copies, L1 bypassed), finds each token's page
+// and an empty split costs one atomic instead of a thread block. Each of the
+// 4 warps streams its own 16-token chunks through a 2-stage cp.async pipeline
+// (16-byte copies, L1 bypassed; two CTAs per SM at d = 128, set by registers), finds each token's page
 // through the block table, and runs the two small products on the tensor
 // cores with mma.sync (S = Q K^T with the group's heads as the 16 rows,
 // O += P V with P kept in registers). Each warp keeps its own running (m, l, O)
@@ -26,7 +27,7 @@ namespace {
 
 constexpr int kChunk = 16;   // tokens per warp per pipeline stage
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kStages = 2;
 
 template <int D>
 struct DecodeLayout {
