@@ -51,6 +51,10 @@ def parse():
                     help="skip the block-sparse, paged, masked and FP8 prefill and backward measurements "
                          "(outside the step)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the cpu_baseline sample")
+    ap.add_argument("--cpu-leg-seconds", type=float, default=6.0,
+                    help="budget of the oracle timed beside each of the other legs (decode, long GQA, varlen)")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the long-context GQA and ragged varlen prefill measurements (outside the step)")
     ap.add_argument("--profile-once", action="store_true",
                     help="one launch each of prefill, decode, block-sparse, paged, masked and FP8 prefill "
                          "and backward on the bench workloads, then exit (for ncu)")
@@ -65,6 +69,8 @@ KERNEL_SOURCES["prefill_tc_kernel<128, sparse>"] = KERNEL_SOURCES["prefill_tc_ke
 KERNEL_SOURCES["prefill_tc_kernel<128, paged>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["prefill_tc_kernel<128, masked>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["prefill_tc_kernel<128, fp8>"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["prefill_tc_kernel<128>, long GQA"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
+KERNEL_SOURCES["prefill_tc_kernel<64>, varlen"] = KERNEL_SOURCES["prefill_tc_kernel<128>"]
 KERNEL_SOURCES["bwd_dkdv_kernel<128>"] = ["backward.cu", "sm100_primitives.cuh", "device_common.cuh", "fattn_internal.h"]
 KERNEL_SOURCES["bwd_dq_kernel<128>"] = KERNEL_SOURCES["bwd_dkdv_kernel<128>"]
 
@@ -355,6 +361,90 @@ def fp8_leg(fattn, pre, flush, stream, peaks, dev):
             "launches": 2, "traffic": recorded_traffic("prefill_tc_kernel<128, fp8>")}
 
 
+def cpu_baseline_rows(x, seconds: float, what: str, chunk: int = 64):
+    """Time the fp64 oracle on random chunks of query rows of a causal prefill workload
+    (dense [B, N, H, d] or varlen [T, H, d] with cu_seqlens), on the host cores."""
+    import numpy as np
+    from oracle import attention as orc
+    rng = np.random.default_rng(0)
+    varlen = x.cu_seqlens is not None
+    d = x.q.shape[-1]
+    if varlen:
+        cu = [int(c) for c in x.cu_seqlens]
+        lens = [cu[b + 1] - cu[b] for b in range(len(cu) - 1)]
+        H = x.q.shape[1]
+    else:
+        B, N, H = x.q.shape[0], x.q.shape[1], x.q.shape[2]
+        lens = [N] * B
+    done_rows, flops, t_used, groups = 0, 0.0, 0.0, 0
+    while t_used < seconds:
+        b, h = int(rng.integers(len(lens))), int(rng.integers(H))
+        n = min(chunk, lens[b])
+        rows = np.sort(rng.choice(lens[b], size=n, replace=False))
+        smp = np.stack([np.full(n, b), np.full(n, h), rows], axis=1)
+        t0 = time.perf_counter()
+        if varlen:
+            orc.attn_fwd_rows(x.q, x.k, x.v, x.scale, True, smp, cu_seqlens=x.cu_seqlens)
+        else:
+            orc.attn_fwd_rows(x.q, x.k, x.v, x.scale, True, smp)
+        t_used += time.perf_counter() - t0
+        flops += float(np.sum(4.0 * d * (rows + 1)))      # causal: row i sees i+1 keys
+        done_rows += n
+        groups += 1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": flops / t_used / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done_rows} query rows ({groups} random (sequence, head) groups of up to {chunk} rows) "
+                      f"of the {what}, fp64 numpy (BLAS threads = cores), {t_used:.1f} s"}
+
+
+def prefill_config_leg(fattn, x, what, kernel, flush, stream, peaks, dev, cpu_seconds):
+    """fattn_fwd on one more prefill workload (10 launches, median, L2 flushed before each),
+    with its roofline against the measured bf16 burst peak and the oracle timed beside it."""
+    import torch
+    q, k, v = x.q.to(dev), x.k.to(dev), x.v.to(dev)
+    o = torch.empty_like(q)
+    if x.cu_seqlens is not None:
+        cu = x.cu_seqlens.to(dev)
+        lse = torch.empty((q.shape[1], q.shape[0]), dtype=torch.float32, device=dev)
+        run = lambda: fattn.fwd(q, k, v, causal=True, scale=x.scale, cu_seqlens=cu, max_seqlen=x.max_seqlen,
+                                out=o, lse=lse)
+    else:
+        lse = torch.empty((q.shape[0], q.shape[2], q.shape[1]), dtype=torch.float32, device=dev)
+        run = lambda: fattn.fwd(q, k, v, causal=True, scale=x.scale, out=o, lse=lse)
+    t = _time_launches(run, flush, stream)
+    tf = x.flops() / (t * 1e-3) / 1e12
+    res = {"workload": what, "ms": t, "tflops": tf, "flops": x.flops(),
+           "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": tf / peaks["bf16_tflops"], "traffic": recorded_traffic(kernel),
+                        "peak_source": "measured bf16_tflops (burst)", "kernel": kernel}}
+    del q, k, v, o, lse
+    if cpu_seconds > 0:
+        res["cpu_baseline"] = cpu_baseline_rows(x, cpu_seconds, what)
+    return res
+
+
+def cpu_baseline_decode(dec, seconds: float):
+    """Time the fp64 oracle's paged decode on the host cores, one sequence of the decode
+    workload at a time (in order) until the budget is spent; KV bytes read per second."""
+    from oracle import attention as orc
+    t_used, kv, seqs, toks = 0.0, 0.0, 0, 0
+    for b in range(dec.batch):
+        if t_used >= seconds:
+            break
+        sl = dec.seqlens[b:b + 1]
+        t0 = time.perf_counter()
+        orc.decode_paged(dec.q[b:b + 1], dec.kcache, dec.vcache, dec.block_table[b:b + 1], sl, dec.scale)
+        t_used += time.perf_counter() - t0
+        n = int(sl[0])
+        kv += 2.0 * n * dec.hkv * dec.d * 2
+        seqs += 1
+        toks += n
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": kv / t_used / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{seqs} of the {dec.batch} decode sequences ({toks} context tokens, all {dec.hq} query "
+                      f"heads), paged gather + fp64 definition in numpy, {t_used:.1f} s"}
+
+
 def cpu_baseline_prefill(pre, seconds: float):
     """Time the fp64 oracle on sampled query rows of the prefill workload."""
     import numpy as np
@@ -452,6 +542,7 @@ def main():
         fattn.decode_paged(dq, dk, dv, dbt, dsl, S, scale=dec.scale, out=do, lse=dlse, workspace=ws)
 
     if args.profile_once:
+        from exact_tiled_attention_fattn_gb300 import inputs
         prefill()
         decode()
         if not args.no_sparse:  # one block-sparse launch: local (3 blocks) + global mask
@@ -462,13 +553,18 @@ def main():
             pa = [t.to(dev) for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q)]
             fattn.fwd_paged(*pa, max(x.lengths_q), causal=True, scale=x.scale)
             fattn.fwd_masked(q, k, v, alibi_mask(pre.q.shape[1], dev), causal=True, scale=pre.scale)  # masked
-            from exact_tiled_attention_fattn_gb300 import inputs
             x8 = inputs.prefill_fp8(1, *pre.q.shape[:3], pre.hkv, pre.q.shape[3], True)  # and FP8
             fattn.fwd_fp8(x8.q8.to(dev), x8.k8.to(dev), x8.v8.to(dev), x8.q_descale, x8.k_descale, x8.v_descale,
                           causal=True, scale=x8.scale)
             do = torch.randn(q.shape, device=dev).to(torch.bfloat16)  # and one backward
             prefill()
             fattn.bwd(q, k, v, o, lse, do, causal=True, scale=pre.scale)
+        if not args.no_configs:  # one long-context GQA and one varlen prefill launch
+            xg = inputs.long_gqa_config()
+            fattn.fwd(xg.q.to(dev), xg.k.to(dev), xg.v.to(dev), causal=True, scale=xg.scale)
+            xv = inputs.varlen_config()
+            fattn.fwd(xv.q.to(dev), xv.k.to(dev), xv.v.to(dev), causal=True, scale=xv.scale,
+                      cu_seqlens=xv.cu_seqlens.to(dev), max_seqlen=xv.max_seqlen)
         torch.cuda.synchronize()
         st = fattn.debug_read_status()
         print(json.dumps({"profile_once": True, "num_splits": S, "device_status": st}), flush=True)
@@ -608,10 +704,19 @@ def main():
     backward = None if args.no_sparse else backward_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev)
     masked = None if args.no_sparse else masked_leg(fattn, pre, q, k, v, o, lse, flush, stream, peaks, dev)
     fp8 = None if args.no_sparse else fp8_leg(fattn, pre, flush, stream, peaks, dev)
+    cpu_s = 0.0 if (rank != 0 or world != 1 or args.no_cpu_baseline) else args.cpu_leg_seconds
+    from exact_tiled_attention_fattn_gb300 import inputs as _inputs
+    long_gqa = None if args.no_configs else prefill_config_leg(
+        fattn, _inputs.long_gqa_config(), "long-context GQA causal prefill B=1 Hq=32 Hkv=8 N=32768 d=128 (seed 2)",
+        "prefill_tc_kernel<128>, long GQA", flush, stream, peaks, dev, cpu_s)
+    varlen = None if args.no_configs else prefill_config_leg(
+        fattn, _inputs.varlen_config(), "ragged varlen causal prefill, 16 sequences U[128,2048] (seed 3, T=13794) "
+        "Hq=Hkv=16 d=64", "prefill_tc_kernel<64>, varlen", flush, stream, peaks, dev, cpu_s)
 
-    cpu = None
+    cpu = cpu_dec = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_prefill(pre, args.cpu_seconds)
+        cpu_dec = cpu_baseline_decode(dec, args.cpu_leg_seconds)
 
     if rank != 0:
         if world > 1:
@@ -642,8 +747,11 @@ def main():
         "decode": {"value": world * gbs, "unit": "GB/s", "ms": t_dec, "kv_bytes": kv_bytes,
                    "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak_b, "unit": "GB/s",
                                 "frac": gbs / peak_b, "traffic": recorded_traffic("decode_kernel<128, page16>"),
-                                "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel<128, page16>"}},
+                                "peak_source": f"{peak_src} hbm_gbs", "kernel": "decode_kernel<128, page16>"},
+                   "cpu_baseline": cpu_dec},
         "prefill_ms": t_pre,
+        "long_gqa_prefill": long_gqa,
+        "varlen_prefill": varlen,
         "block_sparse": sparse,
         "paged_prefill": paged,
         "backward": backward,

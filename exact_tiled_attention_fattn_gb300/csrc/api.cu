@@ -17,6 +17,18 @@ __device__ int g_status_word = 0;
 
 static std::atomic<int*> g_status_ptr[128];
 
+// Test hook of the bounded pipeline waits (fattn_debug_set_wait_limit): the limit of
+// every wait of later tensor-core launches (0 = kDefaultWaitNs) and the stall flag.
+static std::atomic<unsigned long long> g_wait_limit_ns{0};
+static std::atomic<int> g_debug_stall{0};
+
+template <typename Params>
+void set_waits(Params& p) {
+  const unsigned long long w = g_wait_limit_ns.load(std::memory_order_relaxed);
+  p.wait_ns = w ? w : kDefaultWaitNs;
+  p.debug_stall = g_debug_stall.load(std::memory_order_relaxed);
+}
+
 int* status_ptr(int* err) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) {
@@ -131,6 +143,7 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
   p.causal = causal ? 1 : 0; p.scale = scale;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
 
   cudaError_t e;
   if (dtype == FATTN_FP32) {
@@ -172,6 +185,7 @@ extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, con
   p.mask_heads = mask_heads;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
   CUtensorMap tq, tk, tv;
   if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
       !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
@@ -208,6 +222,7 @@ extern "C" fattn_status fattn_fwd_masked(const void* q, const void* k, const voi
   p.mask = mask; p.mask_sb = mask_batch_stride; p.mask_sh = mask_head_stride; p.mask_ld = mask_row_stride;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
   CUtensorMap tq, tk, tv;
   if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
       !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
@@ -249,6 +264,7 @@ extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const
   p.page_size = page_size; p.max_pages = max_pages_per_seq; p.num_pages = num_pages;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
   CUtensorMap tq, tk, tv;
   const int pool_rows = num_pages * page_size;
   if (!encode_rows_map(&tq, q, total_q, Hq, d, 128) || !encode_rows_map(&tk, kcache, pool_rows, Hkv, d, page_size) ||
@@ -299,6 +315,7 @@ extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* 
   p.v_descale = v_descale;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
   uint8_t* vt = static_cast<uint8_t*>(workspace);
   if (launch_fp8_transpose_v(static_cast<const uint8_t*>(v), vt, B, N, Hkv, d, (int)npad, stream) != cudaSuccess)
     return FATTN_ERR_CUDA;
@@ -347,6 +364,7 @@ extern "C" fattn_status fattn_bwd(const void* q, const void* k, const void* v, c
   p.causal = causal ? 1 : 0; p.scale = scale;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
+  set_waits(p);
   CUtensorMap tq, tk, tv, tdo;
   if (!encode_rows_map(&tq, q, (int)rows, Hq, d, 128) || !encode_rows_map(&tk, k, (int)rows, Hkv, d, 128) ||
       !encode_rows_map(&tv, v, (int)rows, Hkv, d, 128) || !encode_rows_map(&tdo, dout, (int)rows, Hq, d, 128))
@@ -429,4 +447,9 @@ extern "C" fattn_status fattn_debug_read_status(cudaStream_t stream) {
   if (cudaMemcpy(&h, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FATTN_ERR_CUDA;
   if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FATTN_ERR_CUDA;
   return static_cast<fattn_status>(h);
+}
+
+extern "C" void fattn_debug_set_wait_limit(unsigned long long limit_ns, int stall) {
+  g_wait_limit_ns.store(limit_ns, std::memory_order_relaxed);
+  g_debug_stall.store(stall ? 1 : 0, std::memory_order_relaxed);
 }

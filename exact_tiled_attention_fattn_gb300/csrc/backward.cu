@@ -54,7 +54,6 @@ constexpr int BT = 128;          // rows of every tile (query rows or keys)
 constexpr int kThreads = 384;   // warps 0-3 control, 4-7 and 8-11 element-wise
 constexpr int kEwArrivals = 8;  // element-wise warps arriving on a barrier
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
 // TMEM columns (both passes): S or S^T at 0 (P / P^T in bf16 over its first 64
 // columns), dP or dP^T at 128 (dS in bf16 over its first 64), accumulators at 256.
@@ -67,9 +66,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          uint64_t limit_ns) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, limit_ns);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -289,7 +289,8 @@ struct DkdvLayout {
   static constexpr int kStages = 2;
   static constexpr int kOffBar = kOffRing + kStages * kStage;
   static constexpr int kNumBars = 13;
-  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
+  static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
@@ -318,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
       mbar_init(bar(i), (i == kPFull || i == kDsFull || i == kAccEmpty) ? kEwArrivals : 1);
+    mbar_init(bar(Lay::kBarStall), 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -356,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, hkv, j;
         item(it, b, hkv, j);
-        if (!mbar_wait(bar(kKvEmpty), (nkv & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kKvEmpty), (nkv & 1) ^ 1, abort, p.status, p.wait_ns)) break;
         mbar_arrive_expect_tx(bar(kKvFull), 2 * Lay::kTile);
         load_tile<D>(sb + Lay::kOffK, &tk, bar(kKvFull), hkv, b * p.N + j * BT, pol_kv);
         load_tile<D>(sb + Lay::kOffV, &tv, bar(kKvFull), hkv, b * p.N + j * BT, pol_kv);
@@ -365,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < G * ni; ++t) {
           const int h = hkv * G + t / ni, i = i0 + t % ni;
           const uint32_t st = nqd & 1, base = sb + Lay::kOffRing + st * Lay::kStage;
-          if (!mbar_wait(bar(kQdEmpty + st), ((nqd >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kQdEmpty + st), ((nqd >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -396,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b, hkv, j;
         item(it, b, hkv, j);
         const int i0 = p.causal ? j : 0, steps = G * (nt - i0);
-        if (!mbar_wait(bar(kKvFull), nkv & 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kKvFull), nkv & 1, abort, p.status, p.wait_ns)) break;
         ++nkv;
         tc_fence_after();
         bool s_issued = false;  // S^T of step t already issued (early, in step t - 1)
@@ -406,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t qmn = smem_desc_sw128(base, BT * 128, 1024);
           const uint64_t domn = smem_desc_sw128(base + Lay::kTile, BT * 128, 1024);
           if (!s_issued) {
-            if (!mbar_wait(bar(kQdFull + st), (nqd >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+            if (!mbar_wait(bar(kQdFull + st), (nqd >> 1) & 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -416,11 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issue_kk<D>(tDP, vd, dok);  // dP^T = V dO^T (dS^T of the previous step was read by its dK product)
           mma_commit(bar(kDpFull));
-          if (t == 0 && !mbar_wait(bar(kAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          if (t == 0 && !mbar_wait(bar(kAccEmpty), (nacc & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(bar(kPFull), np & 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kPFull), np & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -441,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               s_issued = true;
             }
           }
-          if (!mbar_wait(bar(kDsFull), nds & 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kDsFull), nds & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -471,6 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t nqd = 0, ns = 0, ndp = 0, nacc = 0;
     bool ok = true;
+    // test hook: a wait that runs out (nothing arrives on the stall barrier), after which
+    // every role stops, drains and frees TMEM; the outputs stay unwritten
+    if (p.debug_stall && !warp_wait(bar(Lay::kBarStall), 0, abort, p.status, p.wait_ns)) ok = false;
     for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
       int b, hkv, j;
       item(it, b, hkv, j);
@@ -479,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + t % ni;
         const uint32_t st = nqd & 1;
         const float* vec = reinterpret_cast<const float*>(smem + Lay::kOffRing + st * Lay::kStage + 2 * Lay::kTile);
-        if (!warp_wait(bar(kSFull), ns & 1, abort, p.status)) {
+        if (!warp_wait(bar(kSFull), ns & 1, abort, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kPFull));
-        if (!warp_wait(bar(kDpFull), ndp & 1, abort, p.status)) {
+        if (!warp_wait(bar(kDpFull), ndp & 1, abort, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -533,7 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) break;
       // epilogue: warpgroup 0 writes dV, warpgroup 1 scale * dK, one key row per thread
-      if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status)) break;
+      if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status, p.wait_ns)) break;
       ++nacc;
       tc_fence_after();
       const int key = j * BT + r;
@@ -567,7 +572,8 @@ struct DqLayout {
   static constexpr int kOffV = kOffK + kKStages * kTile;
   static constexpr int kOffBar = kOffV + kVStages * kTile;
   static constexpr int kNumBars = 20;
-  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
+  static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
@@ -600,6 +606,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
       mbar_init(bar(i), (i == kQSFree || i == kQDpFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
+    mbar_init(bar(Lay::kBarStall), 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -639,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
         int b, h, i;
         item(it, b, h, i);
-        if (!mbar_wait(bar(kQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kQEmpty), (nq & 1) ^ 1, abort, p.status, p.wait_ns)) break;
         mbar_arrive_expect_tx(bar(kQFull), 2 * Lay::kTile);
         load_tile<D>(sb + Lay::kOffQ, &tq, bar(kQFull), h, b * p.N + i * BT, pol_q);
         load_tile<D>(sb + Lay::kOffDO, &tdo, bar(kQFull), h, b * p.N + i * BT, pol_q);
@@ -647,14 +654,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int jn = p.causal ? i + 1 : nt, hkv = h / G;
         for (int j = 0; j < jn; ++j) {
           const uint32_t ks = nk % 3, vs = nv & 1;
-          if (!mbar_wait(bar(kKEmpty + ks), ((nk / 3) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kKEmpty + ks), ((nk / 3) & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(bar(kKFull + ks), Lay::kTile);
           load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kKFull + ks), hkv, b * p.N + j * BT, pol_kv);
           ++nk;
-          if (!mbar_wait(bar(kVEmpty + vs), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kVEmpty + vs), ((nv >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -692,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto v_addr = [&](uint32_t t) -> uint32_t { return sb + Lay::kOffV + (t & 1) * Lay::kTile; };
       // S_t = Q K_t^T
       auto issue_s = [&](uint32_t t) -> bool {
-        if (!mbar_wait(bar(kKFull + t % 3), (t / 3) & 1, abort, p.status, kWaitLimitNs)) return false;
+        if (!mbar_wait(bar(kKFull + t % 3), (t / 3) & 1, abort, p.status, p.wait_ns)) return false;
         tc_fence_after();
         issue_kk<D>(tS, qd, smem_desc_sw128(k_addr(t), 16, 1024));
         mma_commit(bar(kQSFull));
@@ -700,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // dP_t = dO V_t^T, then V_t's stage is free
       auto issue_dp = [&](uint32_t t) -> bool {
-        if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1, abort, p.status, kWaitLimitNs)) return false;
+        if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1, abort, p.status, p.wait_ns)) return false;
         tc_fence_after();
         issue_kk<D>(tDP, dod, smem_desc_sw128(v_addr(t), 16, 1024));
         mma_commit(bar(kQDpFull));
@@ -711,27 +718,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b, h, i;
         item(it, b, h, i);
         const int jn = p.causal ? i + 1 : nt;
-        if (!mbar_wait(bar(kQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kQFull), nq & 1, abort, p.status, p.wait_ns)) break;
         ++nq;
         if (!issue_s(n) || !issue_dp(n)) break;
         for (int j = 0; j < jn; ++j, ++n) {
           if (j + 1 < jn) {
-            if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs) || !issue_s(n + 1)) {
+            if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, p.wait_ns) || !issue_s(n + 1)) {
               ok = false;
               break;
             }
             ++nfree;
-            if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, kWaitLimitNs) || !issue_dp(n + 1)) {
+            if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns) || !issue_dp(n + 1)) {
               ok = false;
               break;
             }
             ++ndpf;
           }
-          if (j == 0 && !mbar_wait(bar(kQAccEmpty), (nacc & 1) ^ 1, abort, p.status, kWaitLimitNs)) {
+          if (j == 0 && !mbar_wait(bar(kQAccEmpty), (nacc & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
-          if (!mbar_wait(bar(kQDsFull), n & 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kQDsFull), n & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -741,8 +748,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // the item's last S and dP were read before its last dS was written
-        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, kWaitLimitNs) ||
-            !mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, kWaitLimitNs))
+        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, p.wait_ns) ||
+            !mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns))
           break;
         ++nfree;
         ++ndpf;
@@ -765,6 +772,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t ns = 0, ndp = 0, nacc = 0;
     bool ok = true;
+    // test hook: a wait that runs out (nothing arrives on the stall barrier), after which
+    // every role stops, drains and frees TMEM; the outputs stay unwritten
+    if (p.debug_stall && !warp_wait(bar(Lay::kBarStall), 0, abort, p.status, p.wait_ns)) ok = false;
     for (int kk = 0, it; ok && (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
       int b, h, i;
       item(it, b, h, i);
@@ -774,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float nl2 = p.ws_nl2[vrow], dval = p.ws_d[vrow];
       const uint64_t nl2x2 = f2_pack(nl2, nl2);
       for (int j = 0; j < jn; ++j) {
-        if (!warp_wait(bar(kQSFull), ns & 1, abort, p.status)) {
+        if (!warp_wait(bar(kQSFull), ns & 1, abort, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -797,7 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[c + 1] = c + 1 < lim ? ex2(x1) : 0.f;
           }
         }
-        if (!warp_wait(bar(kQDpFull), ndp & 1, abort, p.status)) {
+        if (!warp_wait(bar(kQDpFull), ndp & 1, abort, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -823,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(bar(kQDsFull));
       }
       if (!ok) break;
-      if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status)) break;
+      if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status, p.wait_ns)) break;
       ++nacc;
       tc_fence_after();
       // warpgroup g writes columns [g D / 2, (g + 1) D / 2) of its row

@@ -12,6 +12,9 @@ namespace fattn {
 // Device status word codes (match fattn_status).
 enum : int { kStatusOk = 0, kStatusTimeout = 5, kStatusDeviceCheck = 6 };
 
+// Limit of one pipeline wait unless a test sets another (fattn_debug_set_wait_limit).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
+
 // Problem description shared by both prefill kernels.
 struct PrefillParams {
   const void* q;
@@ -43,6 +46,11 @@ struct PrefillParams {
   // (the tv tensor map); scale already holds scale * q_descale * k_descale
   int fp8;
   float v_descale;
+  // bounded pipeline waits: each mbarrier wait gives up after wait_ns; debug_stall != 0
+  // (test hook) makes the softmax / element-wise warps first wait on a barrier that no
+  // role arrives on, so that the wait runs out and every role takes the abort exit
+  unsigned long long wait_ns;
+  int debug_stall;
 };
 
 // V [B, N, Hkv, d] (E4M3 bytes) -> V^T [B * Hkv, d, Npad], zero past N (d = 128).
@@ -109,6 +117,11 @@ struct BwdParams {
   int causal;
   float scale;
   int* status;
+  // bounded pipeline waits: each mbarrier wait gives up after wait_ns; debug_stall != 0
+  // (test hook) makes the softmax / element-wise warps first wait on a barrier that no
+  // role arrives on, so that the wait runs out and every role takes the abort exit
+  unsigned long long wait_ns;
+  int debug_stall;
 };
 
 // Preprocess, dK/dV pass and dQ pass, in that order on `stream`. Tensor maps

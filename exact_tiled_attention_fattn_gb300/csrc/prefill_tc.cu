@@ -83,7 +83,6 @@ constexpr int kRegsControlMasked = 88;
 constexpr int kRegsSoftmaxMasked = 208;
 static_assert(128 * kRegsControlMasked + 256 * kRegsSoftmaxMasked <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s per wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
 constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exceed it by <= 2^8
 
@@ -127,7 +126,8 @@ struct TcLayout {
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
   static constexpr int kOffBar = kOffV + kStages * kKVBytes;
   static constexpr int kNumBars = kEarly ? kBarCount : kBarSFree;
-  static constexpr int kOffHolder = kOffBar + kNumBars * 8;
+  static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
+  static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffMask = kOffAbort + 8;  // block-mask ring (block-sparse variant)
   // FP8 variant: P_A, P_B as E4M3 128 x 128 tiles in shared memory (128-byte swizzle)
@@ -265,9 +265,10 @@ __device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
 
 // Warp-uniform wait: lane 0 polls, the verdict is broadcast so that every
 // lane takes the same path into the warp-collective tcgen05.ld/st.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status) {
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, int* status,
+                                          uint64_t limit_ns) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, kWaitLimitNs);
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity, abort, status, limit_ns);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   return ok;
 }
@@ -302,6 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(i), (i == kBarPFull || i == kBarPFull + 1 || i == kBarSFree || i == kBarSFree + 1) ? 4
                         : (i >= kBarMaskEmpty && i < kBarMaskEmpty + kMaskSlots)                ? kMaskConsumers
                                                                                                  : 1);
+    mbar_init(bar(Lay::kBarStall), 1);
     *abort = 0;
     fence_mbar_init();
   }
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = max(x.n[0], x.n[1]);
         const uint32_t* mw = nullptr;
         if constexpr (kSparse) {
-          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, kWaitLimitNs))
+          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, p.wait_ns))
             break;
           mw = mask_slot(nm);
           if ((int)mw[2 * kMaskWords + 2] < 0) {  // neither tile keeps a block: Q is not needed
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
         }
-        if (!mbar_wait(bar(kBarQEmpty), (nq & 1) ^ 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kBarQEmpty), (nq & 1) ^ 1, abort, p.status, p.wait_ns)) break;
         if (leader) {
           mbar_arrive_expect_tx(bar(kBarQFull), 2 * Lay::kQBytes);
 #pragma unroll
@@ -400,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto load_k = [&](int j) -> bool {
           const uint32_t st = nk & 1;
-          if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
+          if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) return false;
           // a lane's copy may complete before the leader's expect: the phase still needs the leader's arrival
           if (leader) mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
           issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j, false);
@@ -409,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         auto load_v = [&](int j) -> bool {
           const uint32_t st = nv & 1;
-          if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, kWaitLimitNs)) return false;
+          if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) return false;
           if (leader) mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
           issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j, true);
           ++nv;
@@ -483,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar(kBarSFull + t));
       };
       auto issue_pv = [&](int t, uint32_t vst, bool acc) -> bool {
-        if (!mbar_wait(bar(kBarPFull + t), np[t] & 1, abort, p.status, kWaitLimitNs)) return false;
+        if (!mbar_wait(bar(kBarPFull + t), np[t] & 1, abort, p.status, p.wait_ns)) return false;
         ++np[t];
         tc_fence_after();
         const uint32_t p_tmem = tmem + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t)), o_tmem = tmem + Lay::col_o(t);
@@ -511,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kSparse) {
           // walk the blocks either tile keeps: per block j, O_t += P_t(prev) V_prev for each tile
           // that kept the previous block, then S_t = Q_t K_j^T for each tile that keeps j
-          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, kWaitLimitNs))
+          if (!mbar_wait(bar(kBarMaskFull + nm % kMaskSlots), (nm / kMaskSlots) & 1, abort, p.status, p.wait_ns))
             break;
           const uint32_t* mw = mask_slot(nm);
           const int cnt[2] = {(int)mw[2 * kMaskWords], (int)mw[2 * kMaskWords + 1]};
@@ -521,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++nm;
             continue;
           }
-          if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
+          if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, p.wait_ns)) break;
           ++nq;
           tc_fence_after();
           const int n = max(x.n[0], x.n[1]);
@@ -532,8 +534,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = walk.next(); j >= 0; j = walk.next()) {
             const bool a0 = walk.kept(0), a1 = walk.kept(1);
             const uint32_t kst = nk & 1, vst = nv & 1;
-            if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
-                (!first && !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs))) {
+            if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
+                (!first && !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns))) {
               ok = false;
               break;
             }
@@ -561,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!ok) break;
           const uint32_t vst = nv & 1;
-          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
+          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (had0) {
             if (!issue_pv(0, vst, done0 > 0)) break;
@@ -579,14 +581,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int nA = x.n[0], nB = x.n[1];
         const int n = max(nA, nB);
-        if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, kWaitLimitNs)) break;
+        if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, p.wait_ns)) break;
         ++nq;
         tc_fence_after();
         if constexpr (kEarly) {
           // per K/V tile j: S_A(j) and S_B(j) once each softmax has read its previous S,
           // then O_t += P_t(j-1) V_{j-1} once P_t(j-1) is written
           auto early_s = [&](int t, uint32_t kst) -> bool {
-            if (si[t] > 0 && !mbar_wait(bar(kBarSFree + t), (si[t] - 1) & 1, abort, p.status, kWaitLimitNs))
+            if (si[t] > 0 && !mbar_wait(bar(kBarSFree + t), (si[t] - 1) & 1, abort, p.status, p.wait_ns))
               return false;
             ++si[t];
             tc_fence_after();
@@ -601,7 +603,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j <= n; ++j) {
             if (j < n) {
               const uint32_t kst = nk & 1;
-              if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
+              if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
                   (j < nA && !early_s(0, kst)) || (j < nB && !early_s(1, kst))) {
                 ok = false;
                 break;
@@ -612,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (j > 0) {
               const uint32_t vst = nv & 1;
-              if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+              if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns)) {
                 ok = false;
                 break;
               }
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // j = 0
         {
           const uint32_t kst = nk & 1;
-          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
+          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           issue_s(0, kst);
           if (nB > 0) issue_s(1, kst);
@@ -640,8 +642,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int j = 1; ok && j < n; ++j) {
           const uint32_t kst = nk & 1, vst = nv & 1;
-          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, kWaitLimitNs) ||
-              !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) {
+          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
+              !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -666,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tail: the last P V of each tile
         {
           const uint32_t vst = nv & 1;
-          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, kWaitLimitNs)) break;
+          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (n - 1 < nA) {
             if (!issue_pv(0, vst, n - 1 > 0)) break;
@@ -695,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (it < 0) break;
       const Item x = decode_item(p, sch, it);
       if (!x.valid) continue;
-      if (!warp_wait(bar(kBarMaskEmpty + nm % kMaskSlots), ((nm / kMaskSlots) & 1) ^ 1, abort, p.status)) break;
+      if (!warp_wait(bar(kBarMaskEmpty + nm % kMaskSlots), ((nm / kMaskSlots) & 1) ^ 1, abort, p.status, p.wait_ns)) break;
       uint32_t* w = reinterpret_cast<uint32_t*>(smem + Lay::kOffMask + (nm % kMaskSlots) * kMaskSlotBytes);
       const int nw = (max(x.n[0], x.n[1]) + 31) >> 5;   // <= kMaskWords: nb <= kSparseMaxBlocks
       int cnt[2] = {0, 0}, last = -1;
@@ -748,6 +750,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_col = tmem + lane_off + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t));
     uint32_t nm = 0;                         // block-mask slots consumed
     bool ok = true;
+    // test hook: a wait that runs out (nothing arrives on the stall barrier), after which
+    // every role stops, drains and frees TMEM; the outputs stay unwritten
+    if (p.debug_stall && !warp_wait(bar(Lay::kBarStall), 0, abort, p.status, p.wait_ns)) ok = false;
     for (int k = 0; ok; ++k) {
       const int it = item_index(sch, k);
       if (it < 0) break;
@@ -757,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kept_blocks = x.n[t];
       if constexpr (kSparse) {
         const uint32_t mb = bar(kBarMaskFull + nm % kMaskSlots), mp = (nm / kMaskSlots) & 1;
-        if (!warp_wait(mb, mp, abort, p.status)) break;
+        if (!warp_wait(mb, mp, abort, p.status, p.wait_ns)) break;
         mbar_try_wait(mb, mp);  // completed: this lane's own acquire of the mask words
         mw = mask_slot(nm);
         kept_blocks = (int)mw[2 * kMaskWords + t];
@@ -809,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c8 = 0; c8 < BN / 16; ++c8) load_mask(c8);
         }
-        if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status)) {
+        if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status, p.wait_ns)) {
           ok = false;
           break;
         }
@@ -939,7 +944,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kEarly) {
           // O_t += P_t(j-1) V has completed: O_t may be rescaled and P_t's buffer rewritten
           if (!first) {
-            if (!warp_wait(bar(kBarPvDone + t), npv & 1, abort, p.status)) {
+            if (!warp_wait(bar(kBarPvDone + t), npv & 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -986,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       release_mask();
       // epilogue: O / l in bf16 and the row's logsumexp
-      if (!warp_wait(bar(kEarly ? kBarPvDone + t : kBarOFull + t), (kEarly ? npv : no) & 1, abort, p.status)) {
+      if (!warp_wait(bar(kEarly ? kBarPvDone + t : kBarOFull + t), (kEarly ? npv : no) & 1, abort, p.status, p.wait_ns)) {
         ok = false;
         break;
       }

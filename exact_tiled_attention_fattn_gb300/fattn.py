@@ -48,6 +48,7 @@ SIGNATURES = {
     "fattn_merge_partials": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp]),
     "fattn_status_string": (ctypes.c_char_p, [_i]),
     "fattn_debug_read_status": (_i, [_vp]),
+    "fattn_debug_set_wait_limit": (None, [ctypes.c_ulonglong, _i]),
 }
 
 _lib = None
@@ -397,6 +398,8 @@ def decode_paged(q, kcache, vcache, block_table, seqlens, num_splits: int, scale
     _need_cuda(q, kcache, vcache, block_table, seqlens, out, lse, workspace)
     if block_table.dtype != torch.int32 or seqlens.dtype != torch.int32:
         raise TypeError("block_table and seqlens must be int32")
+    if not (q.dtype == kcache.dtype == vcache.dtype == torch.bfloat16):
+        raise TypeError("q, kcache and vcache must be bfloat16 (the decode kernels read bf16 only)")
     B, Hq, d = q.shape
     num_pages, page_size, Hkv, _ = kcache.shape
     _expect(kcache, (num_pages, page_size, Hkv, d), "kcache")
@@ -438,6 +441,8 @@ def decode_paged_static(q, kcache, vcache, block_table, seqlens, num_splits: int
     _need_cuda(q, kcache, vcache, block_table, seqlens, out, lse)
     if block_table.dtype != torch.int32 or seqlens.dtype != torch.int32:
         raise TypeError("block_table and seqlens must be int32")
+    if not (q.dtype == kcache.dtype == vcache.dtype == torch.bfloat16):
+        raise TypeError("q, kcache and vcache must be bfloat16 (the decode kernels read bf16 only)")
     B, Hq, d = q.shape
     num_pages, page_size, Hkv, _ = kcache.shape
     _expect(kcache, (num_pages, page_size, Hkv, d), "kcache")
@@ -495,3 +500,11 @@ def merge_partials(o_part, lse_part, out_dtype=torch.bfloat16, out=None, lse=Non
 def debug_read_status(stream=None) -> int:
     """Synchronise the stream, then read and clear the device status word."""
     return int(load_library().fattn_debug_read_status(ctypes.c_void_p(_stream_handle(stream))))
+
+
+def debug_set_wait_limit(limit_ns: int = 0, stall: bool = False) -> None:
+    """Test hook: limit of every pipeline wait in later tensor-core launches (0 = the
+    default, 2 s); with ``stall`` their softmax / element-wise warps first wait on a
+    barrier nothing arrives on, so each launch times out (FATTN_ERR_TIMEOUT) and
+    returns without writing its outputs. Reset with debug_set_wait_limit(0, False)."""
+    load_library().fattn_debug_set_wait_limit(int(limit_ns), 1 if stall else 0)

@@ -325,6 +325,25 @@ const char* fattn_status_string(fattn_status status);
  */
 fattn_status fattn_debug_read_status(cudaStream_t stream);
 
+/*
+ * fattn_debug_set_wait_limit — test hook for the bounded pipeline waits of the
+ * tensor-core kernels (every prefill variant and the backward passes; decode and
+ * the fp32 prefill have no such waits). The pages have no counterpart: this is
+ * library plumbing for failure tests.
+ *
+ * Every mbarrier wait of those kernels gives up after a limit (default 2 s):
+ * it records FATTN_ERR_TIMEOUT in the device status word, every role of the
+ * kernel stops, copies and tensor-core products already issued are waited for,
+ * TMEM is freed and the kernel returns, so the CUDA context stays usable.
+ * limit_ns > 0 sets that limit for launches made after this call (0 restores the
+ * default). stall != 0 makes the softmax / element-wise warps of those launches
+ * first wait on a barrier that no role ever arrives on, so the wait runs out after
+ * limit_ns: the launch then writes none of its outputs and the status word reads
+ * FATTN_ERR_TIMEOUT. The setting is process-wide and not synchronised with
+ * launches in flight on other host threads; reset it with (0, 0).
+ */
+void fattn_debug_set_wait_limit(unsigned long long limit_ns, int stall);
+
 #ifdef __cplusplus
 }
 #endif

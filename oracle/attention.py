@@ -68,6 +68,7 @@ __all__ = [
     "decode_paged",
     "attn_fwd_paged",
     "attn_bwd",
+    "attn_bwd_rows",
     "attn_fwd_masked",
     "e4m3_to_f64",
     "attn_fwd_fp8",
@@ -215,10 +216,10 @@ def attn_fwd_masked(q, k, v, scale: float, causal: bool, mask, rows=None):
         rows = np.asarray(rows, dtype=np.int64)
         o = np.zeros((len(rows), v.shape[-1]))
         lse = np.zeros(len(rows))
-        for n, (b, h, i) in enumerate(rows):
-            ob, lb = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
-                                          rows=[int(i)], bias=mb(b, h))
-            o[n], lse[n] = ob[0], lb[0]
+        for b, h in sorted({(int(b), int(h)) for b, h, _ in rows}):
+            idx = np.nonzero((rows[:, 0] == b) & (rows[:, 1] == h))[0]
+            o[idx], lse[idx] = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
+                                                    rows=rows[idx, 2], bias=mb(b, h))
         return o, lse
     o = np.zeros(q.shape[:3] + (v.shape[-1],))
     lse = np.zeros((B, Hq, N))
@@ -322,11 +323,11 @@ def attn_fwd_block_sparse(q, k, v, scale: float, causal: bool, block_mask, block
     rows = np.asarray(rows, dtype=np.int64)
     o = np.zeros((len(rows), v.shape[-1]))
     lse = np.zeros(len(rows))
-    for n, (b, h, i) in enumerate(rows):
+    for b, h in sorted({(int(b), int(h)) for b, h, _ in rows}):   # each head's visibility formed once
+        idx = np.nonzero((rows[:, 0] == b) & (rows[:, 1] == h))[0]
         allow = block_sparse_allowed(bm[h % bm.shape[0]], N, N, block)
-        ob, lb = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
-                                      rows=np.array([i]), allowed=allow)
-        o[n], lse[n] = ob[0], lb[0]
+        o[idx], lse[idx] = attention_definition(q[b, :, h], k[b, :, h // g], v[b, :, h // g], scale, causal,
+                                                rows=rows[idx, 2], allowed=allow)
     return o, lse
 
 
@@ -514,6 +515,51 @@ def attn_bwd(q, k, v, do, scale: float, causal: bool):
             ds = p * (dp - dmat[:, None])                            # dS = P o (dP - D)
             dq[b, :, h] = scale * (ds @ kh)                          # dQ = scale dS K
             dk[b, :, h // g] += scale * (ds.T @ q[b, :, h])          # dK = scale dS^T Q
+    return dq, dk, dv
+
+
+def attn_bwd_rows(q, k, v, do, scale: float, causal: bool, dq_rows, dkv_rows):
+    """Selected rows of the gradients of attn_bwd, for sizes too large to form whole.
+
+    Same steps as attn_bwd ([FA-PAPER] "The backward pass recomputes instead of
+    reading"), per (b, query head) with the whole head as one block: P, O = P V and
+    D = rowsum(dO o O) are formed for the head, then only the requested rows of
+    dQ = scale dS K (rows of dS) and the requested key rows of dV = P^T dO and
+    dK = scale dS^T Q (columns of P and dS) are taken.
+    dq_rows: int [n, 3] of (b, query head h, row i) -> dQ[b, i, h];
+    dkv_rows: int [m, 3] of (b, KV head g, key row j) -> dK[b, j, g], dV[b, j, g],
+    each summed over the query heads that share KV head g.
+    Returns (dq [n, d], dk [m, d], dv [m, dv]).
+    """
+    dq_rows = np.asarray(dq_rows, dtype=np.int64).reshape(-1, 3)
+    dkv_rows = np.asarray(dkv_rows, dtype=np.int64).reshape(-1, 3)
+    B, N, Hq, d = q.shape
+    Hkv = k.shape[2]
+    g = Hq // Hkv
+    dq = np.zeros((len(dq_rows), d))
+    dk = np.zeros((len(dkv_rows), d))
+    dv = np.zeros((len(dkv_rows), v.shape[-1]))
+    heads = {(int(b), int(h)) for b, h, _ in dq_rows}
+    heads |= {(int(b), int(hk) * g + r) for b, hk, _ in dkv_rows for r in range(g)}
+    for b, h in sorted(heads):
+        qh, kh, vh = _f64(q[b, :, h]), _f64(k[b, :, h // g]), _f64(v[b, :, h // g])
+        dOh = _f64(do[b, :, h])
+        p = attention_weights(qh, kh, scale, causal)                  # [N, N]
+        dmat = np.sum(dOh * (p @ vh), axis=1)                          # D = rowsum(dO o O)
+        iq = np.nonzero((dq_rows[:, 0] == b) & (dq_rows[:, 1] == h))[0]
+        if len(iq):
+            rows = dq_rows[iq, 2]
+            dp = dOh[rows] @ vh.T                                      # dP rows = dO_i V^T
+            ds = p[rows] * (dp - dmat[rows, None])                     # dS rows
+            dq[iq] = scale * (ds @ kh)                                 # dQ_i = scale dS_i K
+        ikv = np.nonzero((dkv_rows[:, 0] == b) & (dkv_rows[:, 1] == h // g))[0]
+        if len(ikv):
+            cols = dkv_rows[ikv, 2]
+            pc = p[:, cols]                                            # P[:, j]
+            dv[ikv] += pc.T @ dOh                                      # dV_j = P[:, j]^T dO
+            dpc = dOh @ vh[cols].T                                     # dP[:, j] = dO V_j
+            dsc = pc * (dpc - dmat[:, None])                           # dS[:, j]
+            dk[ikv] += scale * (dsc.T @ qh)                            # dK_j = scale dS[:, j]^T Q
     return dq, dk, dv
 
 

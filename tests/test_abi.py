@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
                           "fattn_bwd_workspace_size", "fattn_decode_workspace_size",
                           "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
-                          "fattn_debug_read_status"}
+                          "fattn_debug_read_status", "fattn_debug_set_wait_limit"}
 
 
 def test_status_strings(lib):

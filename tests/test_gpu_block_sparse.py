@@ -6,7 +6,7 @@ import torch
 
 from exact_tiled_attention_fattn_gb300 import inputs
 from oracle import attention as orc
-from tests.gpu_util import as_np, check, need_gpu
+from tests.gpu_util import as_np, check, nan_outputs, need_gpu, tile_edge_samples
 
 pytestmark = pytest.mark.gpu
 BLK = 128
@@ -76,8 +76,10 @@ def test_lower_triangular_blocks_with_causal_equal_causal(fa):
     check(o, lse, o_ref, lse_ref, what="tril blocks")
 
 
-def test_local_global_pattern_large_sampled(fa):
-    """B=1, H=32, N=4096, d=128: sliding window of 3 blocks plus the first block (~17% dense)."""
+def test_local_global_pattern_large_every_item(fa):
+    """B=1, H=32, N=4096, d=128: sliding window of 3 blocks plus the first block (~17% dense),
+    on NaN-filled outputs: every row written, both edge rows of every (head, 128-row
+    tile) and random rows against the oracle."""
     B, N, H, d = 1, 4096, 32, 128
     x = inputs.prefill_dense(3300, B, N, H, H, d, causal=True)
     nb = N // BLK
@@ -85,9 +87,12 @@ def test_local_global_pattern_large_sampled(fa):
     for i in range(nb):
         m[0, i, max(0, i - 2): i + 1] = 1
         m[0, i, 0] = 1
-    o, lse = _run(fa, x, m, True)
-    rng = np.random.default_rng(5)
-    smp = np.array([(0, int(rng.integers(H)), int(rng.integers(N))) for _ in range(128)] + [(0, 0, 0), (0, 31, N - 1)])
+    o, lse = nan_outputs(x.q.shape, (B, H, N))
+    fa.fwd_block_sparse(x.q.cuda(), x.k.cuda(), x.v.cuda(), torch.from_numpy(m).cuda(), causal=True,
+                        scale=x.scale, out=o, lse=lse)
+    assert fa.debug_read_status() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), "rows left unwritten (NaN)"
+    smp = tile_edge_samples(B, H, N, np.random.default_rng(5), extra=128)
     o_ref, lse_ref = orc.attn_fwd_block_sparse(x.q, x.k, x.v, x.scale, True, m, BLK, rows=smp)
     hi = torch.as_tensor(smp[:, 1], device="cuda")
     ii = torch.as_tensor(smp[:, 2], device="cuda")

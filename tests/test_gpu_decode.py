@@ -156,3 +156,15 @@ def test_workspace_reused_across_calls(fa):
         assert fa.debug_read_status() == 0
         o_ref, lse_ref = orc.decode_paged(x.q, x.kcache, x.vcache, x.block_table, x.seqlens, x.scale)
         check(o, lse, o_ref, lse_ref, what=f"reuse seed {seed} S {S}")
+
+
+def test_binding_rejects_non_bf16_decode_inputs(fa):
+    """The decode kernels read bf16 only and the C ABI carries no dtype: the binding refuses
+    fp32 q or caches in both decode entry points instead of reading them as bf16 pairs."""
+    x = inputs.decode_paged(90, 2, 8, 2, 128, 16, None, 64, spare_pages=1, lengths=[10, 40])
+    q, kc, vc, bt, sl = (t.cuda() for t in (x.q, x.kcache, x.vcache, x.block_table, x.seqlens))
+    for args in ((q.float(), kc, vc), (q, kc.float(), vc), (q, kc, vc.float())):
+        with pytest.raises(TypeError):
+            fa.decode_paged(*args, bt, sl, 2, scale=x.scale)
+        with pytest.raises(TypeError):
+            fa.decode_paged_static(*args, bt, sl, 2, scale=x.scale)

@@ -6,7 +6,7 @@ import torch
 
 from exact_tiled_attention_fattn_gb300 import inputs
 from oracle import attention as orc
-from tests.gpu_util import as_np, check, need_gpu
+from tests.gpu_util import as_np, check, nan_outputs, need_gpu, tile_edge_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -61,17 +61,19 @@ def test_lower_triangle_mask_equals_causal(fa):
     check(o2, l2, o_ref, lse_ref, what="causal")
 
 
-def test_alibi_bias_large_sampled(fa):
-    """B=4, H=32, N=4096, d=128, causal, one shared bias M[i, j] = -0.01 (i - j): sampled rows."""
+def test_alibi_bias_large_every_item(fa):
+    """B=4, H=32, N=4096, d=128, causal, one shared bias M[i, j] = -0.01 (i - j), on
+    NaN-filled outputs: every row written, both edge rows of every (sequence, head,
+    128-row tile) and random rows against the oracle."""
     B, N, H, d = 4, 4096, 32, 128
     x = inputs.prefill_dense(5300, B, N, H, H, d, True)
     i = torch.arange(N, dtype=torch.float32)
     m = (-0.01 * (i[:, None] - i[None, :])).to(torch.bfloat16)[None, None]
-    o, lse = fa.fwd_masked(x.q.cuda(), x.k.cuda(), x.v.cuda(), m.cuda(), causal=True, scale=x.scale)
+    o, lse = nan_outputs(x.q.shape, (B, H, N))
+    fa.fwd_masked(x.q.cuda(), x.k.cuda(), x.v.cuda(), m.cuda(), causal=True, scale=x.scale, out=o, lse=lse)
     assert fa.debug_read_status() == 0
-    rng = np.random.default_rng(9)
-    smp = np.array([(int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(N))) for _ in range(96)] +
-                   [(0, 0, 0), (3, 31, N - 1)])
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), "rows left unwritten (NaN)"
+    smp = tile_edge_samples(B, H, N, np.random.default_rng(9), extra=96)
     o_ref, lse_ref = orc.attn_fwd_masked(x.q, x.k, x.v, x.scale, True, m.float().numpy(), rows=smp)
     bi, hi, ii = (torch.as_tensor(smp[:, c], device="cuda") for c in range(3))
     check(o[bi, ii, hi], lse[bi, hi, ii], o_ref, lse_ref, what="ALiBi-style bias")

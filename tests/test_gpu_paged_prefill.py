@@ -6,7 +6,7 @@ import torch
 
 from exact_tiled_attention_fattn_gb300 import inputs
 from oracle import attention as orc
-from tests.gpu_util import as_np, check, need_gpu
+from tests.gpu_util import as_np, check, nan_outputs, need_gpu, tile_edge_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -58,22 +58,26 @@ def test_full_prefill_from_cache_equals_varlen_bitwise(fa):
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def test_chunked_prefill_large_sampled(fa):
+def test_chunked_prefill_large_every_item(fa):
     """B=4, Hq=32, Hkv=8, d=128, 16-token pages, contexts U[4096, 16384], a 2048-query
-    chunk at the end of each context: sampled rows against the oracle."""
+    chunk at the end of each context, on NaN-filled outputs: every row written, both
+    edge rows of every (sequence, head, 128-row tile) and random rows against the oracle."""
     x = inputs.prefill_paged(710, 4, 32, 8, 128, 16, (4096, 16384), 2048, 16384, causal=True)
-    o, lse = _run(fa, x)
+    Tq = x.q.shape[0]
+    o, lse = nan_outputs(x.q.shape, (32, Tq))
+    _run(fa, x, out=o, lse=lse)
     assert fa.debug_read_status() == 0
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all(), "rows left unwritten (NaN)"
     rng = np.random.default_rng(7)
-    smp = [(b, int(rng.integers(32)), int(rng.integers(x.lengths_q[b]))) for b in range(4) for _ in range(24)]
-    smp += [(0, 0, 0), (3, 31, x.lengths_q[3] - 1)]
+    smp = [(b, h, i) for b in range(4) for h in range(32) for i in tile_edge_rows(x.lengths_q[b])]
+    smp += [(b, int(rng.integers(32)), int(rng.integers(x.lengths_q[b]))) for b in range(4) for _ in range(24)]
     smp = np.array(smp)
     o_ref, lse_ref = orc.attn_fwd_paged(x.q, x.kcache, x.vcache, x.block_table, x.seqlens_k, x.cu_seqlens_q,
                                         x.scale, True, samples=smp)
     cu = x.cu_seqlens_q.tolist()
     rows = torch.as_tensor([cu[b] + i for b, _, i in smp], device="cuda")
     heads = torch.as_tensor(smp[:, 1], device="cuda")
-    check(o[rows, heads], lse[heads, rows], o_ref, lse_ref, what="chunked prefill sampled")
+    check(o[rows, heads], lse[heads, rows], o_ref, lse_ref, what="chunked prefill")
 
 
 def test_bad_table_entry_and_seqlen_are_reported(fa):

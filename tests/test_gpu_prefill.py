@@ -7,7 +7,7 @@ import torch
 
 from exact_tiled_attention_fattn_gb300 import inputs
 from oracle import attention as orc
-from tests.gpu_util import check, need_gpu, as_np
+from tests.gpu_util import as_np, check, nan_outputs, need_gpu, tile_edge_samples
 
 pytestmark = pytest.mark.gpu
 
@@ -205,38 +205,48 @@ def test_output_guards_untouched(fa):
     check(o, lse, o_ref, lse_ref, what="guarded")
 
 
-# ------------------------------------------------------------ the full-size workloads (sampled rows)
-def _samples(rng, B, Hq, N, n=256):
-    s = [(int(rng.integers(B)), int(rng.integers(Hq)), int(rng.integers(N))) for _ in range(n)]
-    for i in (0, 1, 127, 128, 129, N // 2, N - 129, N - 128, N - 1):
-        s.append((int(rng.integers(B)), int(rng.integers(Hq)), i))
-    return np.array(s)
-
-
-def _sampled_check(fa, x, what):
-    o, lse = _run(fa, x)
+# ------------------------------------------------------------ the full-size workloads
+def _full_size_check(fa, x, what):
+    """The launch the bench times, on NaN-filled outputs: every row must be written
+    (finite), causal row 0 must be V[0] bit for bit, and the oracle is compared at
+    both edge rows of every (sequence, head, 128-row tile) plus random rows, so every
+    work item of the schedule (each a pair of tiles) is checked."""
     B, N, Hq = x.q.shape[0], x.q.shape[1], x.q.shape[2]
-    smp = _samples(np.random.default_rng(N), B, Hq, N)
-    o_ref, lse_ref = orc.attn_fwd_rows(x.q, x.k, x.v, x.scale, x.causal, smp)
-    bi = torch.as_tensor(smp[:, 0], device="cuda")
-    hi = torch.as_tensor(smp[:, 1], device="cuda")
-    ii = torch.as_tensor(smp[:, 2], device="cuda")
-    check(o[bi, ii, hi], lse[bi, hi, ii], o_ref, lse_ref, what=what)
-    # properties that hold at any size: finite everywhere, causal row 0 is V[0] exactly
-    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    o, lse = nan_outputs(x.q.shape, (B, Hq, N))
+    fa.fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), causal=x.causal, scale=x.scale, out=o, lse=lse)
+    assert fa.debug_read_status() == 0
+    assert torch.isfinite(o.float()).all(), f"{what}: rows left unwritten (NaN)"
+    assert torch.isfinite(lse).all(), f"{what}: lse entries left unwritten (NaN)"
     G = x.hq // x.hkv
     v0 = x.v[:, 0].cuda()[:, torch.arange(Hq, device="cuda") // G]
     assert torch.equal(o[:, 0], v0)
+    smp = tile_edge_samples(B, Hq, N, np.random.default_rng(N))
+    o_ref, lse_ref = orc.attn_fwd_rows(x.q, x.k, x.v, x.scale, x.causal, smp)
+    bi, hi, ii = (torch.as_tensor(smp[:, c], device="cuda") for c in range(3))
+    check(o[bi, ii, hi], lse[bi, hi, ii], o_ref, lse_ref, what=what)
 
 
-def test_causal_mha_config_sampled(fa):
+def test_causal_mha_config_every_item(fa):
     """B=4, Hq=Hkv=32, N=4096, d=128, causal, seed 1 (the benchmarked launch)."""
-    _sampled_check(fa, inputs.causal_mha_config(), "causal MHA config")
+    _full_size_check(fa, inputs.causal_mha_config(), "causal MHA config")
 
 
-def test_long_gqa_config_sampled(fa):
+def test_long_gqa_config_every_item(fa):
     """B=1, Hq=32, Hkv=8, N=32768, d=128, causal, seed 2."""
-    _sampled_check(fa, inputs.long_gqa_config(), "long GQA config")
+    _full_size_check(fa, inputs.long_gqa_config(), "long GQA config")
+
+
+def test_varlen_config_nan_filled(fa):
+    """The varlen workload (16 packed sequences, H=16, d=64) on NaN-filled outputs:
+    every row written, every row equal to the oracle."""
+    x = inputs.varlen_config()
+    T, H = x.q.shape[0], x.q.shape[1]
+    o, lse = nan_outputs(x.q.shape, (H, T))
+    fa.fwd(x.q.cuda(), x.k.cuda(), x.v.cuda(), causal=True, scale=x.scale, cu_seqlens=x.cu_seqlens.cuda(),
+           max_seqlen=x.max_seqlen, out=o, lse=lse)
+    assert fa.debug_read_status() == 0
+    o_ref, lse_ref = _ref(x)
+    check(o, lse, o_ref, lse_ref, what="varlen config (NaN-filled outputs)")
 
 
 def _jump_inputs(N, H, d, jumps, step, seed):

@@ -398,7 +398,7 @@ def test_block_sparse_all_ones_is_dense_and_empty_rows():
     bm[0, 1, :] = 0                                   # query block 1 sees nothing
     o, lse = orc.attn_fwd_block_sparse(q, k, v, 0.3, False, bm, blk)
     assert np.all(o[:, blk:2 * blk] == 0) and np.all(np.isneginf(lse[:, :, blk:2 * blk]))
-    smp = np.array([[1, 3, 9], [0, 0, 5], [1, 2, 0]])
+    smp = np.array([[1, 3, 9], [0, 0, 5], [1, 2, 0], [1, 3, 2], [0, 0, 5], [1, 3, 1]])
     os_, ls_ = orc.attn_fwd_block_sparse(q, k, v, 0.3, False, bm, blk, rows=smp)
     for n, (b, h, i) in enumerate(smp):
         assert np.array_equal(os_[n], o[b, i, h]) or np.max(np.abs(os_[n] - o[b, i, h])) <= 1e-14
@@ -529,6 +529,40 @@ def test_backward_closed_form_uniform_causal():
     assert np.max(np.abs(dq)) <= 1e-13 and np.max(np.abs(dk)) <= 1e-13
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_equal_whole_gradients(causal):
+    """attn_bwd_rows (the sampled form used at full size) equals the pinned attn_bwd at
+    the requested rows, GQA included (dK, dV summed over the query heads of a group),
+    with rows repeated and in any order; and one of its dK rows matches central
+    differences of L = sum(O o dO) directly."""
+    rng = np.random.default_rng(43)
+    B, N, Hq, Hkv, d, sc = 2, 11, 4, 2, 5, 0.45
+    q, k, v = _rand(rng, B, N, Hq, d), _rand(rng, B, N, Hkv, d), _rand(rng, B, N, Hkv, d)
+    do = _rand(rng, B, N, Hq, d)
+    dq, dk, dv = orc.attn_bwd(q, k, v, do, sc, causal)
+    rq = np.array([[0, 0, 0], [1, 3, 10], [0, 2, 5], [1, 3, 10], [1, 1, 7]])
+    rkv = np.array([[0, 1, 0], [1, 0, 10], [1, 1, 4], [0, 0, 9], [0, 1, 0]])
+    sq, sk, sv = orc.attn_bwd_rows(q, k, v, do, sc, causal, rq, rkv)
+    for n, (b, h, i) in enumerate(rq):
+        assert np.max(np.abs(sq[n] - dq[b, i, h])) <= 1e-13
+    for n, (b, g, j) in enumerate(rkv):
+        assert np.max(np.abs(sk[n] - dk[b, j, g])) <= 1e-13
+        assert np.max(np.abs(sv[n] - dv[b, j, g])) <= 1e-13
+    # central differences on dK[1, 4, 1]
+    eps = 1e-6
+    for c in range(d):
+        old = k[1, 4, 1, c]
+        k[1, 4, 1, c] = old + eps
+        lp = _loss(q, k, v, do, sc, causal)
+        k[1, 4, 1, c] = old - eps
+        lm = _loss(q, k, v, do, sc, causal)
+        k[1, 4, 1, c] = old
+        assert abs((lp - lm) / (2 * eps) - sk[2, c]) <= 1e-7
+    # no rows requested: empty results
+    e = orc.attn_bwd_rows(q, k, v, do, sc, causal, np.zeros((0, 3)), np.zeros((0, 3)))
+    assert e[0].shape == (0, d) and e[1].shape == (0, d) and e[2].shape == (0, d)
+
+
 def test_additive_mask_vs_python_loops():
     """O = softmax(scale Q K^T + M) V with a general additive M (-inf entries remove keys)."""
     rng = np.random.default_rng(50)
@@ -570,7 +604,7 @@ def test_additive_mask_special_cases():
     o3, l3 = orc.attn_fwd_masked(q, k, v, sc, False, np.broadcast_to(c, (1, H, N, N)))
     assert np.max(np.abs(o3 - o0)) <= 1e-13
     assert np.max(np.abs(l3 - (l0 + c[0, :, :, 0][None]))) <= 1e-13
-    smp = np.array([[0, 1, 3], [0, 0, 8]])
+    smp = np.array([[0, 1, 3], [0, 0, 8], [0, 1, 0], [0, 1, 3], [0, 0, 2]])
     os_, ls_ = orc.attn_fwd_masked(q, k, v, sc, False, tri, rows=smp)
     for n, (b, h, i) in enumerate(smp):
         assert np.max(np.abs(os_[n] - o2[b, i, h])) <= 1e-15 and abs(ls_[n] - l2[b, h, i]) <= 1e-15

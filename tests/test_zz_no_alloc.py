@@ -12,7 +12,8 @@ import pytest
 import torch
 
 from exact_tiled_attention_fattn_gb300 import inputs
-from tests.gpu_util import check, need_gpu, as_np
+from oracle import attention as orc
+from tests.gpu_util import as_np, check, need_gpu
 
 
 def _dev(x):
@@ -21,6 +22,8 @@ def _dev(x):
 
 @pytest.mark.gpu
 def test_static_scratch_decode_matches_workspace_decode_twice():
+    """Two calls in a row with different shapes: each output equals the workspace entry
+    point's (same kernels) and the fp64 oracle's, within the bf16 tolerances."""
     fa = need_gpu()
     cases = [
         (inputs.decode_paged(61, 4, 16, 4, 128, 16, (100, 9000), 9216, spare_pages=4), 16),
@@ -28,10 +31,12 @@ def test_static_scratch_decode_matches_workspace_decode_twice():
     ]
     for x, S in cases:                                   # two calls in a row, different shapes
         q, kc, vc, bt, sl = _dev(x)
-        o_ref, l_ref = fa.decode_paged(q, kc, vc, bt, sl, S, scale=x.scale)
+        o_ws, l_ws = fa.decode_paged(q, kc, vc, bt, sl, S, scale=x.scale)
         o, l = fa.decode_paged_static(q, kc, vc, bt, sl, S, scale=x.scale)
         assert fa.debug_read_status() == 0
-        check(o, l, as_np(o_ref), as_np(l_ref), what=f"static scratch S={S}")
+        check(o, l, as_np(o_ws), as_np(l_ws), what=f"static scratch vs workspace S={S}")
+        o_ref, l_ref = orc.decode_paged(x.q, x.kcache, x.vcache, x.block_table, x.seqlens, x.scale)
+        check(o, l, o_ref, l_ref, what=f"static scratch vs oracle S={S}")
 
 
 @pytest.mark.gpu
