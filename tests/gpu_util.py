@@ -28,6 +28,8 @@ def need_gpu():
 
 
 def as_np(t):
+    if isinstance(t, np.ndarray):
+        return t.astype(np.float64)
     return t.detach().float().cpu().double().numpy()
 
 
