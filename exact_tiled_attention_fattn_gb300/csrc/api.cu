@@ -149,13 +149,13 @@ extern "C" fattn_status fattn_fwd(const void* q, const void* k, const void* v, v
   if (dtype == FATTN_FP32) {
     e = launch_prefill_f32(p, stream);
   } else {
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tv, to;
     if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
-        !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+        !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128) || !encode_rows_map(&to, o, p.total_rows, Hq, d, 32))
       return FATTN_ERR_CUDA;
     int sms = num_sms_current();
     if (sms <= 0) return FATTN_ERR_CUDA;
-    e = launch_prefill_tc(p, tq, tk, tv, sms, stream);
+    e = launch_prefill_tc(p, tq, tk, tv, to, sms, stream);
   }
   return e == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
@@ -186,13 +186,13 @@ extern "C" fattn_status fattn_fwd_block_sparse(const void* q, const void* k, con
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
-      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128) || !encode_rows_map(&to, o, p.total_rows, Hq, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;
-  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, to, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void* o, float* lse, int B,
@@ -223,13 +223,13 @@ extern "C" fattn_status fattn_fwd_masked(const void* q, const void* k, const voi
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_rows_map(&tq, q, p.total_rows, Hq, d, 128) || !encode_rows_map(&tk, k, p.total_rows, Hkv, d, 128) ||
-      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128))
+      !encode_rows_map(&tv, v, p.total_rows, Hkv, d, 128) || !encode_rows_map(&to, o, p.total_rows, Hq, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;
-  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, to, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const void* vcache,
@@ -265,14 +265,14 @@ extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   const int pool_rows = num_pages * page_size;
   if (!encode_rows_map(&tq, q, total_q, Hq, d, 128) || !encode_rows_map(&tk, kcache, pool_rows, Hkv, d, page_size) ||
-      !encode_rows_map(&tv, vcache, pool_rows, Hkv, d, page_size))
+      !encode_rows_map(&tv, vcache, pool_rows, Hkv, d, page_size) || !encode_rows_map(&to, o, total_q, Hq, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;
-  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, to, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -319,14 +319,15 @@ extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* 
   uint8_t* vt = static_cast<uint8_t*>(workspace);
   if (launch_fp8_transpose_v(static_cast<const uint8_t*>(v), vt, B, N, Hkv, d, (int)npad, stream) != cudaSuccess)
     return FATTN_ERR_CUDA;
-  CUtensorMap tq, tk, tv;
+  CUtensorMap tq, tk, tv, to;
   if (!encode_u8_map(&tq, q, d, Hq, rows, (uint64_t)d, (uint64_t)Hq * d, 128, 1, 128) ||
       !encode_u8_map(&tk, k, d, Hkv, rows, (uint64_t)d, (uint64_t)Hkv * d, 128, 1, 128) ||
-      !encode_u8_map(&tv, vt, npad, d, (uint64_t)B * Hkv, (uint64_t)npad, (uint64_t)npad * d, 128, 128, 1))
+      !encode_u8_map(&tv, vt, npad, d, (uint64_t)B * Hkv, (uint64_t)npad, (uint64_t)npad * d, 128, 128, 1) ||
+      !encode_rows_map(&to, o, (int)rows, Hq, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;
-  return launch_prefill_tc(p, tq, tk, tv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_prefill_tc(p, tq, tk, tv, to, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" size_t fattn_bwd_workspace_size(int B, int Hq, int N) {

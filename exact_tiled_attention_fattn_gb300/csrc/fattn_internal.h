@@ -61,9 +61,10 @@ cudaError_t launch_fp8_transpose_v(const uint8_t* v, uint8_t* vt, int B, int N, 
 constexpr int kSparseMaxBlocks = 2048;
 
 // Tensor-core prefill (bf16 in, fp32 accumulate, bf16 out). Tensor maps are
-// encoded by the caller over the packed [rows, H, d] views of q, k and v.
+// encoded by the caller over the packed [rows, H, d] views of q, k and v (128-row
+// boxes) and of o (bf16, 32-row boxes: the epilogue's stores).
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tv, int num_sms, cudaStream_t stream);
+                              const CUtensorMap& tv, const CUtensorMap& to, int num_sms, cudaStream_t stream);
 
 // CUDA-core fp32 prefill.
 cudaError_t launch_prefill_f32(const PrefillParams& p, cudaStream_t stream);

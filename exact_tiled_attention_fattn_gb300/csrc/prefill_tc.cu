@@ -124,19 +124,26 @@ struct TcLayout {
   static constexpr int kOffQ = 0;                 // Q_A then Q_B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffV + kStages * kKVBytes;
+  // Epilogue staging (every variant but the block-sparse one, whose mask ring takes the
+  // room): each softmax warp writes its 32 rows of one 64-column half of O (bf16, 128-byte
+  // swizzle) into a 4 KB slot of its own and stores them with one TMA box.
+  static constexpr bool kStageO = kMode != kModeSparse;
+  static constexpr int kStageSlot = 32 * 128;
+  static constexpr int kOffStage = kOffV + kStages * kKVBytes;
+  static constexpr int kOffBar = kOffStage + (kStageO ? 8 * kStageSlot : 0);
   static constexpr int kNumBars = kEarly ? kBarCount : kBarSFree;
   static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
   static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
   static constexpr int kOffMask = kOffAbort + 8;  // block-mask ring (block-sparse variant)
   // FP8 variant: P_A, P_B as E4M3 128 x 128 tiles in shared memory (128-byte swizzle)
-  static constexpr int kOffP = (kOffMask + kMaskSlots * kMaskSlotBytes + 1023) / 1024 * 1024;
+  static constexpr int kOffP = (kOffMask + (kMode == kModeSparse ? kMaskSlots * kMaskSlotBytes : 0) + 1023) / 1024 * 1024;
   static constexpr int kPBytes = kFp8 ? BM * BN : 0;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would block in tcgen05.alloc) never shares the SM
   static constexpr int kUsed = kOffP + 2 * kPBytes + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
+  static_assert(kBytes <= 227 * 1024, "shared memory");
   // TMEM columns: fp32 scores S_A, S_B (bf16 variants: P_X in bf16 over their first 64
   // columns), fp32 O_A, O_B.
   __host__ __device__ static constexpr uint32_t col_s(int t) { return t ? 128u : 0u; }
@@ -278,7 +285,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap to,
+                      const PrefillParams p) {
   constexpr bool kSparse = kMode == kModeSparse;  // fixed block mask, zero blocks skipped
   constexpr bool kPaged = kMode == kModePaged;    // K/V through a block table
   constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
@@ -311,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
+    if constexpr (Lay::kStageO) tma_prefetch_desc(&to);
   }
   if (warp == 1) {
     tmem_alloc(sb + Lay::kOffHolder, kTmemCols);
@@ -1003,19 +1012,54 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool live = row < x.L;
       // a row the mask left with no key: O = 0, lse = -inf
       const float inv = (kMasked && l == 0.f) ? 0.f : (kFp8 ? p.v_descale : 1.f) / l;
-      __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
+      const int wrow0 = x.base + t * BM + q4 * 32;  // this warp's first row
+      if (Lay::kStageO && wrow0 + 32 <= x.L) {
+        // all 32 rows of the warp lie in the sequence: stage each 64-column half in the
+        // warp's slot (row `lane` at 128 lane, 16-byte chunk c at c ^ (lane mod 8): the
+        // 128-byte swizzle of the O tensor map) and store it with one TMA box
+        uint8_t* slot = smem + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
+        const uint32_t slot_s = sb + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(o_col + 32 * c, u);
-        uint32_t w[16];
+        for (int hh = 0; hh < D / 64; ++hh) {
+          if (lane == 0) bulk_wait_read_all();  // the slot's previous store has read it
+          __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+          for (int c2 = 0; c2 < 2; ++c2) {
+            uint32_t u[32];
+            tmem_ld32(o_col + 64 * hh + 32 * c2, u);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 4; ++e) {
+              uint32_t w[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                w[i] = pack_bf16x2(__uint_as_float(u[8 * e + 2 * i]) * inv, __uint_as_float(u[8 * e + 2 * i + 1]) * inv);
+              const int chunk = 4 * c2 + e;
+              *reinterpret_cast<uint4*>(slot + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
+                  make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&to, slot_s, 64 * hh, x.h, x.row0 + wrow0);
+            bulk_commit_group();
+          }
+        }
+      } else {
+        __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.o) + ((size_t)(x.row0 + row) * p.Hq + x.h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(o_col + 32 * c, u);
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
       if (live && p.lse) {
@@ -1028,6 +1072,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // the epilogue's TMA stores complete before the CTA (and its staging slots) goes away
+  if (Lay::kStageO && warp >= 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -1038,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int kMode>
 cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     int num_sms, cudaStream_t stream) {
+                     const CUtensorMap& to, int num_sms, cudaStream_t stream) {
   using Lay = TcLayout<D, kMode>;
   auto kern = prefill_tc_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kBytes);
@@ -1047,29 +1093,29 @@ cudaError_t launch_t(const PrefillParams& p, const CUtensorMap& tq, const CUtens
   const long long items = (long long)p.B * p.Hq * pairs;
   if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
   const int grid = (int)(items < num_sms ? items : num_sms);
-  kern<<<grid, kThreads, Lay::kBytes, stream>>>(tq, tk, tv, p);
+  kern<<<grid, kThreads, Lay::kBytes, stream>>>(tq, tk, tv, to, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill_tc(const PrefillParams& p, const CUtensorMap& tq, const CUtensorMap& tk,
-                              const CUtensorMap& tv, int num_sms, cudaStream_t stream) {
+                              const CUtensorMap& tv, const CUtensorMap& to, int num_sms, cudaStream_t stream) {
   if (p.block_mask) {
-    if (p.d == 128) return launch_t<128, kModeSparse>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, kModeSparse>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, kModeSparse>(p, tq, tk, tv, to, num_sms, stream);
+    return launch_t<64, kModeSparse>(p, tq, tk, tv, to, num_sms, stream);
   }
   if (p.block_table) {
-    if (p.d == 128) return launch_t<128, kModePaged>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, kModePaged>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, kModePaged>(p, tq, tk, tv, to, num_sms, stream);
+    return launch_t<64, kModePaged>(p, tq, tk, tv, to, num_sms, stream);
   }
-  if (p.fp8) return p.d == 128 ? launch_t<128, kModeFp8>(p, tq, tk, tv, num_sms, stream) : cudaErrorInvalidValue;
+  if (p.fp8) return p.d == 128 ? launch_t<128, kModeFp8>(p, tq, tk, tv, to, num_sms, stream) : cudaErrorInvalidValue;
   if (p.mask) {
-    if (p.d == 128) return launch_t<128, kModeMasked>(p, tq, tk, tv, num_sms, stream);
-    return launch_t<64, kModeMasked>(p, tq, tk, tv, num_sms, stream);
+    if (p.d == 128) return launch_t<128, kModeMasked>(p, tq, tk, tv, to, num_sms, stream);
+    return launch_t<64, kModeMasked>(p, tq, tk, tv, to, num_sms, stream);
   }
-  if (p.d == 128) return launch_t<128, kModeDense>(p, tq, tk, tv, num_sms, stream);
-  return launch_t<64, kModeDense>(p, tq, tk, tv, num_sms, stream);
+  if (p.d == 128) return launch_t<128, kModeDense>(p, tq, tk, tv, to, num_sms, stream);
+  return launch_t<64, kModeDense>(p, tq, tk, tv, to, num_sms, stream);
 }
 
 }  // namespace fattn
