@@ -18,7 +18,10 @@
 //               diagonal, sequence end), keeps the running max m and sum l in
 //               registers, writes P (bf16) over the first 64 columns of its S
 //               buffer, rescales O in TMEM when the max moved, and at the end
-//               writes O / l (bf16) and lse = m + ln l.
+//               writes O / l (bf16) and lse = m + ln l. A warp whose 32 rows all
+//               lie in the sequence stages them in shared memory and writes them
+//               with TMA tensor stores (one 32-row box per 64 columns) instead of
+//               one 256-byte row per thread, scattered over rows 8 KB apart.
 // The running max is raised lazily: a row keeps its old m while no new score
 // exceeds it by more than 2^8 (p <= 256 then, exact in the final O/l because O
 // and l use the same m), which makes the O rescale rare.
