@@ -74,9 +74,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 }
 
 // ------------------------------------------------------------------ preprocess
-// Rows of O and dO in memory order ((b, i, h), each d contiguous), kRowsPerWarp
-// at a time per warp with their loads in flight together; each lane reads d / 32
-// elements of both. The padded workspace rows (i >= N) are written by a second loop.
+// A warp takes 32 consecutive query rows i0 .. i0 + 31 of one (sequence, head):
+// lane u reads the row's lse (one 128-byte read per warp), the warp walks the 32
+// rows of O and dO (each a contiguous d-long row; kRowsPerWarp rows with their
+// loads in flight together, each lane d / 32 elements of both), reduces each
+// row's dot product with shuffles and keeps row u's in lane u, and the warp
+// writes both workspace vectors with one 128-byte store each. Rows past N (the
+// padding up to Npad) get -inf and 0.
 constexpr int kRowsPerWarp = 4;
 
 template <int D>
@@ -84,54 +88,47 @@ __global__ void bwd_preprocess_kernel(const BwdParams p) {
   constexpr int E = D / 32;  // elements per lane: 4 (8 bytes) or 2 (4 bytes)
   using Vec = typename std::conditional<E == 4, uint2, uint32_t>::type;
   const int lane = threadIdx.x & 31;
-  const int rows = p.B * p.N * p.Hq;               // < 2^31: checked on the host
+  const int chunks = p.Npad / 32;                   // 32-row blocks per (sequence, head)
+  const int tasks = p.B * p.Hq * chunks;
   const int warps = (int)((gridDim.x * blockDim.x) >> 5);
-  const int warp_id = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout);
-  for (int m0 = warp_id * kRowsPerWarp; m0 < rows; m0 += warps * kRowsPerWarp) {
-    Vec a[kRowsPerWarp], d[kRowsPerWarp];
+  for (int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); task < tasks; task += warps) {
+    const int bh = task / chunks, i0 = (task - bh * chunks) * 32;
+    const int b = bh / p.Hq, h = bh - b * p.Hq;
+    const int i = i0 + lane;                        // this lane's row of the block
+    const float lse = i < p.N ? __ldg(p.lse + (size_t)bh * p.N + i) : -CUDART_INF_F;
+    const int nrows = min(32, p.N - i0);            // rows of the block inside the sequence (may be <= 0)
+    float mine = 0.f;
+    for (int u0 = 0; u0 < nrows; u0 += kRowsPerWarp) {
+      Vec a[kRowsPerWarp], d[kRowsPerWarp];
 #pragma unroll
-    for (int u = 0; u < kRowsPerWarp; ++u) {
-      if (m0 + u < rows) {
-        const size_t off = (size_t)(m0 + u) * D + lane * E;
-        a[u] = __ldg(reinterpret_cast<const Vec*>(o + off));
-        d[u] = __ldg(reinterpret_cast<const Vec*>(g + off));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kRowsPerWarp; ++u) {
-      const int m = m0 + u;
-      if (m >= rows) break;
-      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
-      const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d[u]);
-      float dsum = 0.f;
-#pragma unroll
-      for (int w = 0; w < E / 2; ++w) {
-        dsum = fmaf(bf16_lo(aw[w]), bf16_lo(dw[w]), dsum);
-        dsum = fmaf(bf16_hi(aw[w]), bf16_hi(dw[w]), dsum);
+      for (int u = 0; u < kRowsPerWarp; ++u) {
+        if (u0 + u < nrows) {
+          const size_t off = (((size_t)b * p.N + i0 + u0 + u) * p.Hq + h) * D + lane * E;
+          a[u] = __ldg(reinterpret_cast<const Vec*>(o + off));
+          d[u] = __ldg(reinterpret_cast<const Vec*>(g + off));
+        }
       }
 #pragma unroll
-      for (int s = 16; s > 0; s >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, s);
-      if (lane == 0) {
-        const int h = m % p.Hq, bi = m / p.Hq;
-        const int i = bi % p.N, b = bi / p.N;
-        const int bh = b * p.Hq + h;
-        const float lse = __ldg(p.lse + (size_t)bh * p.N + i);
-        // a row with no visible key (lse = -inf) gets P = 0
-        p.ws_nl2[(size_t)bh * p.Npad + i] = (lse > -CUDART_INF_F && lse < CUDART_INF_F) ? -lse * kLog2e : -CUDART_INF_F;
-        p.ws_d[(size_t)bh * p.Npad + i] = dsum;
+      for (int u = 0; u < kRowsPerWarp; ++u) {
+        if (u0 + u >= nrows) break;
+        const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
+        const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d[u]);
+        float dsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < E / 2; ++w) {
+          dsum = fmaf(bf16_lo(aw[w]), bf16_lo(dw[w]), dsum);
+          dsum = fmaf(bf16_hi(aw[w]), bf16_hi(dw[w]), dsum);
+        }
+#pragma unroll
+        for (int sft = 16; sft > 0; sft >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, sft);
+        if (lane == u0 + u) mine = dsum;
       }
     }
-  }
-  const int pad = p.Npad - p.N;
-  if (pad > 0) {
-    const int total = p.B * p.Hq * pad;
-    for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < total; t += gridDim.x * blockDim.x) {
-      const int bh = t / pad, i = p.N + (t - bh * pad);
-      p.ws_nl2[(size_t)bh * p.Npad + i] = -CUDART_INF_F;  // padded query rows: P = 0
-      p.ws_d[(size_t)bh * p.Npad + i] = 0.f;
-    }
+    // a row with no visible key (lse = -inf), and a padding row, get P = 0
+    p.ws_nl2[(size_t)bh * p.Npad + i] = (lse > -CUDART_INF_F && lse < CUDART_INF_F) ? -lse * kLog2e : -CUDART_INF_F;
+    p.ws_d[(size_t)bh * p.Npad + i] = i < p.N ? mine : 0.f;
   }
 }
 
@@ -857,9 +854,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.N * p.Hq;
-  const long long per_block = 8LL * kRowsPerWarp;
-  const int pre_blocks = (int)std::min<long long>((rows + per_block - 1) / per_block, (long long)num_sms * 16);
+  const long long tasks = (long long)p.B * p.Hq * (p.Npad / 32);  // 32-row blocks, 8 per 256-thread block
+  const int pre_blocks = (int)std::min<long long>((tasks + 7) / 8, (long long)num_sms * 16);
   bwd_preprocess_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
