@@ -68,8 +68,7 @@ constexpr int kThreads = 384;    // 3 warpgroups
 // Register split (setmaxnreg): launched at 168 per thread (65536 / 384, rounded
 // down to the allocation granularity), i.e. 384 * 168 = 64512 in total. The
 // producer/MMA warpgroup drops to 96 and the two softmax warpgroups rise to 200
-// (128 * 96 + 256 * 200 = 63488), the split at which no variant but the masked
-// one spills (88 / 208 left 16-byte spills in the control warps: 1-2 % slower).
+// (128 * 96 + 256 * 200 = 63488), the split at which no d = 128 variant spills (88 / 208 left 16-byte spills in the control warps: 1-2 % slower).
 // The build checks that ptxas launches this kernel at exactly kRegsLaunch.
 constexpr int kRegsLaunch = 168;
 constexpr int kRegsControl = 96;
@@ -81,10 +80,6 @@ static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= kThreads * kRegsLaunch,
 constexpr int kRegsControlSparse = 104;
 constexpr int kRegsSoftmaxSparse = 200;
 static_assert(128 * kRegsControlSparse + 256 * kRegsSoftmaxSparse <= kThreads * kRegsLaunch, "register split");
-// The masked variant holds mask entries in the softmax warps: 128 * 88 + 256 * 208 = 64512.
-constexpr int kRegsControlMasked = 88;
-constexpr int kRegsSoftmaxMasked = 208;
-static_assert(128 * kRegsControlMasked + 256 * kRegsSoftmaxMasked <= kThreads * kRegsLaunch, "register split");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s per drain wait
 constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exceed it by <= 2^8
@@ -337,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = p.Hq / p.Hkv;
 
   if (warp < 4) {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsControlSparse : kMasked ? kRegsControlMasked : kRegsControl));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsControlSparse : kRegsControl));
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // Lane 0 issues every copy; the paged variant runs lanes 0-7 through the same
@@ -745,7 +740,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsSoftmaxSparse : kMasked ? kRegsSoftmaxMasked : kRegsSoftmax));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"((kSparse || Lay::kPTmem) ? kRegsSoftmaxSparse : kRegsSoftmax));
     // ------------------------------------------------------------ softmax (tile t)
     const int t = (warp - 4) >> 2;           // 0: tile A (warps 4-7), 1: tile B (warps 8-11)
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may touch
@@ -761,6 +756,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t npv = 0;                        // O_t += P_t V completions seen (dense d = 64)
     const uint32_t p_col = tmem + lane_off + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t));
     uint32_t nm = 0;                         // block-mask slots consumed
+    // this warp's 4 KB staging slot (the epilogue's O stores; the masked variant's mask rows)
+    uint8_t* slot = smem + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
+    const uint32_t slot_s = sb + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
+    bool slot_store = false;                 // an O store from the slot may still be reading it
     bool ok = true;
     // test hook: a wait that runs out (nothing arrives on the stall barrier), after which
     // every role stops, drains and frees TMEM; the outputs stay unwritten
@@ -817,12 +816,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < x.n[t]; j = kSparse ? walk.next() : j + 1) {
         // the tile's 128 mask entries, requested before waiting for S (16-byte loads
         // of whole 8-key groups; groups at or past the visible limit are not read)
-        uint4 mv[kMasked ? BN / 8 : 1];
+        uint4 mv[kMasked ? BN / 16 : 1];
         auto load_mask = [&](int c8) {
           mv[c8] = j * BN + 8 * c8 < lim ? __ldg(reinterpret_cast<const uint4*>(mrow + j * BN + 8 * c8))
                                          : make_uint4(0u, 0u, 0u, 0u);
         };
-        if constexpr (kMasked) {  // the first half now, the second once S has arrived
+        if constexpr (kMasked) {
+          // the second half of the warp's 32 mask rows (keys 64-127 of the tile) goes to the
+          // warp's staging slot by coalesced 16-byte copies (8 lanes per row, row rr at
+          // 128 rr, chunk c at c ^ (rr mod 8); groups at or past the row's visible limit
+          // are zero-filled without a read); the first half to registers, one row per thread
+          __syncwarp();  // every lane has read the slot's previous contents
+          if (slot_store) {  // an O store from the slot may still be reading it
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            slot_store = false;
+          }
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3), cc = lane & 7;
+            const int qrow = x.base + t * BM + q4 * 32 + rr;
+            const int rlim = p.causal ? min(qrow + x.off + 1, x.Lk) : x.Lk;
+            const int key0 = j * BN + BN / 2 + 8 * cc;
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(p.mask) + (size_t)x.b * p.mask_sb +
+                                       (size_t)x.h * p.mask_sh + (size_t)min(qrow, x.L - 1) * p.mask_ld + key0;
+            cp_async_16(slot_s + rr * 128 + ((cc ^ (rr & 7)) << 4), src, key0 < rlim ? 16u : 0u);
+          }
+          cp_async_commit();
 #pragma unroll
           for (int c8 = 0; c8 < BN / 16; ++c8) load_mask(c8);
         }
@@ -840,17 +860,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           // exponent), one packed FMA per column pair, 32 columns at a time so each
           // mask word dies as its scores arrive; keys past the visible limit -inf
           // (their p is 0 below)
-#pragma unroll
-#pragma unroll
-          for (int c8 = BN / 16; c8 < BN / 8; ++c8) load_mask(c8);
+          cp_async_wait_all();
+          __syncwarp();  // the warp's copies of the second half have landed
 #pragma unroll
           for (int q32 = 0; q32 < BN / 32; ++q32) {
             uint32_t u[32];
             tmem_ld32(s_col + 32 * q32, u);
+            uint4 gq[4];  // this 32-column group's mask entries
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+              const int c8 = 4 * q32 + c4;
+              gq[c4] = c8 < BN / 16 ? mv[c8 < BN / 16 ? c8 : 0]
+                                    : *reinterpret_cast<const uint4*>(slot + lane * 128 + (((c8 - BN / 16) ^ (lane & 7)) << 4));
+            }
 #pragma unroll
             for (int e = 0; e < 32; e += 2) {
               const int c = 32 * q32 + e;
-              const uint4& g = mv[c >> 3];
+              const uint4& g = gq[e >> 3];
               const uint32_t w = ((c & 7) >> 1) == 0 ? g.x : ((c & 7) >> 1) == 1 ? g.y : ((c & 7) >> 1) == 2 ? g.z : g.w;
               float t0, t1;
               f2_unpack(f2_fma(f2_pack(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), scale2,
@@ -1020,8 +1046,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // all 32 rows of the warp lie in the sequence: stage each 64-column half in the
         // warp's slot (row `lane` at 128 lane, 16-byte chunk c at c ^ (lane mod 8): the
         // 128-byte swizzle of the O tensor map) and store it with one TMA box
-        uint8_t* slot = smem + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
-        const uint32_t slot_s = sb + Lay::kOffStage + (warp - 4) * Lay::kStageSlot;
+        slot_store = true;
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh) {
           if (lane == 0) bulk_wait_read_all();  // the slot's previous store has read it
