@@ -133,8 +133,11 @@ __global__ void bwd_preprocess_kernel(const BwdParams p) {
 }
 
 // ------------------------------------------------------------------ work order
-// Items (head, tile) are taken in groups of heads whose items fill about two
-// rounds of the grid; inside a group the items go heaviest tile first (all heads
+// Items (head, tile) are taken in groups of heads whose items fill about four
+// rounds of the grid (measured on the causal MHA workload, B=4 H=32 N=4096: 1.74 ms
+// for the whole backward call against 1.96 with two rounds, 1.86 with one, 1.81 with
+// three or five, 1.84 with six, 1.75 with eight; on the 32k-token GQA one 23.9 against
+// 24.0 ms); inside a group the items go heaviest tile first (all heads
 // of the group at one tile index, then the next), and the grid walks the list in
 // alternating direction round by round ("snake"), so the tiles the CTAs stream
 // (Q and dO in the dK/dV pass, K and V in the dQ pass) belong to a few heads at
@@ -146,7 +149,7 @@ __device__ __forceinline__ BwdSchedule make_bwd_schedule(int heads, int tiles, i
   BwdSchedule s;
   s.tiles = tiles;
   s.heads = heads;
-  int grp = (2 * (int)gridDim.x + tiles - 1) / tiles;
+  int grp = (4 * (int)gridDim.x + tiles - 1) / tiles;
   grp = ((grp + unit - 1) / unit) * unit;
   s.group = grp < heads ? grp : heads;
   s.total = heads * tiles;
