@@ -775,7 +775,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item x = decode_item(p, sch, it);
       if (!x.valid) continue;
       const uint32_t* mw = nullptr;
-      int kept_blocks = x.n[t];
+      // this tile's K/V tile count, selected rather than indexed (a run-time index into the
+      // item's array would put the whole item in local memory)
+      const int nt = t ? x.n[1] : x.n[0];
+      int kept_blocks = nt;
       if constexpr (kSparse) {
         const uint32_t mb = bar(kBarMaskFull + nm % kMaskSlots), mp = (nm / kMaskSlots) & 1;
         if (!warp_wait(mb, mp, abort, p.status, p.wait_ns)) break;
@@ -791,7 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nm;
         }
       };
-      if (x.n[t] == 0) {
+      if (nt == 0) {
         release_mask();
         continue;
       }
@@ -817,8 +820,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kMasked)
         mrow = static_cast<const __nv_bfloat16*>(p.mask) + (size_t)x.b * p.mask_sb + (size_t)x.h * p.mask_sh +
                (size_t)min(row, x.L - 1) * p.mask_ld;
-      BitWalk walk(mw, 1 << t, x.n[t]);
-      for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < x.n[t]; j = kSparse ? walk.next() : j + 1) {
+      BitWalk walk(mw, 1 << t, nt);
+      for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < nt; j = kSparse ? walk.next() : j + 1) {
         // the tile's 128 mask entries, requested before waiting for S (16-byte loads
         // of whole 8-key groups; groups at or past the visible limit are not read)
         uint4 mv[kMasked ? BN / 16 : 1];
