@@ -5,9 +5,8 @@
 // One CTA per SM loops over work items (sequence, query head, 256 query rows =
 // two 128-row Q tiles A and B that share every K/V tile). Roles:
 //   warp 0      TMA producer: Q_A and Q_B once per item, then K_j / V_j tiles
-//               into two 2-stage rings (128-byte swizzle, 64-column boxes). Except
-//               in the block-sparse variant, the K_j and V_{j-1} of one step share
-//               one slot's full / empty barriers.
+//               into two 2-stage rings (128-byte swizzle, 64-column boxes); the
+//               K_j and V_{j-1} of one step share one slot's full / empty barriers.
 //   warp 1      MMA issuer (one thread). Per K/V tile j it issues
 //               O_A += P_A(j-1) V_{j-1}, S_A = Q_A K_j^T, O_B += P_B(j-1) V_{j-1},
 //               S_B = Q_B K_j^T, so that while one softmax warpgroup works on its
@@ -97,13 +96,14 @@ constexpr int kMaskSlotBytes = 2 * kMaskWords * 4 + 16;
 constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8 softmax warps
 static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
-// barrier slots
+// barrier slots (KvFull / KvEmpty: one pair per K/V ring slot, which holds the K tile
+// and the V tile of one step)
 enum : int {
-  kBarQFull = 0, kBarQEmpty = 1, kBarKFull = 2, kBarKEmpty = 4, kBarVFull = 6, kBarVEmpty = 8,
-  kBarSFull = 10, kBarPFull = 12, kBarOFull = 14, kBarMmaDone = 16,
-  kBarMaskFull = 17, kBarMaskEmpty = 17 + kMaskSlots,
+  kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 4,
+  kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarMmaDone = 12,
+  kBarMaskFull = 13, kBarMaskEmpty = 13 + kMaskSlots,
   // separate P buffers (dense d = 64): S_t read by the softmax, O_t += P_t V completed
-  kBarSFree = 17 + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
+  kBarSFree = 13 + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
 };
 
 enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // cannot keep up with the tensor core for small pages.
     const bool leader = lane == 0;
     if (kPaged ? lane < BN / 16 : leader) {
-      uint32_t nq = 0, nk = 0, nv = 0, nm = 0;
+      uint32_t nq = 0, nk = 0, nm = 0;  // nk: K/V ring steps
       const uint64_t pol_q = policy_evict_first(), pol_kv = policy_evict_last();
       for (int k = 0;; ++k) {
         const int it = item_index(sch, k);
@@ -414,63 +414,54 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_3d(dst + dc * BN * 128, map, full, dc * 64, hkv, x.row0 + j * BN, pol_kv);
           }
         };
-        auto load_k = [&](int j) -> bool {
-          const uint32_t st = nk & 1;
-          if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) return false;
-          // a lane's copy may complete before the leader's expect: the phase still needs the leader's arrival
-          if (leader) mbar_arrive_expect_tx(bar(kBarKFull + st), Lay::kKVBytes);
-          issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), j, false);
-          ++nk;
-          return true;
-        };
-        auto load_v = [&](int j) -> bool {
-          const uint32_t st = nv & 1;
-          if (!mbar_wait(bar(kBarVEmpty + st), ((nv >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) return false;
-          if (leader) mbar_arrive_expect_tx(bar(kBarVFull + st), Lay::kKVBytes);
-          issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarVFull + st), j, true);
-          ++nv;
-          return true;
-        };
-        // the order the MMA warp consumes them: K0 K1 V0 K2 V1 K3 V2 ... (over the
-        // blocks either tile visits)
+        // in the order the MMA warp consumes them, one ring slot per step: K0; K1 V0;
+        // K2 V1; ...; V(last) (over the blocks either tile visits)
         bool ok = true;
-        int prev = -1;
         if constexpr (kSparse) {
+          int prev = -1;
+          // the same steps over the union of the blocks either tile keeps: K of this block
+          // and V of the previous kept one, then V of the last one alone
           BitWalk walk(mw, 3, n);
-          for (int j = walk.next(); ok && j >= 0; j = walk.next()) {
-            ok = load_k(j) && (prev < 0 || load_v(prev));
+          for (int j = walk.next(); ok; j = walk.next()) {
+            const uint32_t st = nk & 1;
+            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
+              ok = false;
+              break;
+            }
+            if (leader) mbar_arrive_expect_tx(bar(kBarKvFull + st), ((j >= 0) + (prev >= 0)) * Lay::kKVBytes);
+            if (j >= 0) issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKvFull + st), j, false);
+            if (prev >= 0) issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarKvFull + st), prev, true);
+            ++nk;
+            if (j < 0) break;
             prev = j;
           }
           mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
           ++nm;
         } else {
           // step s: K_s (s < n) and V_{s-1} (s > 0) into slot nk mod 2 of both rings, under
-          // one full / empty barrier pair (the K ring's; step 0 carries K_0 alone, step n
-          // V_{n-1} alone): the MMA issuer takes them in the same step, so it saves a wait
-          // and a commit per step, which the tensor core would otherwise wait out (causal MHA
-          // 0.485 -> 0.479 ms, varlen d = 64 0.127 -> 0.119 ms). The block-sparse walk keeps
-          // separate K and V barriers.
+          // one full / empty barrier pair (step 0 carries K_0 alone, step n V_{n-1} alone):
+          // the MMA issuer takes them in the same step, so it saves a wait and a commit per
+          // step, which the tensor core would otherwise wait out (against separate K and V
+          // barriers: causal MHA 0.485 -> 0.479 ms, varlen d = 64 0.127 -> 0.119 ms)
           for (int s = 0; ok && s <= n; ++s) {
             const uint32_t st = nk & 1;
-            if (!mbar_wait(bar(kBarKEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
+            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
-            if (leader) mbar_arrive_expect_tx(bar(kBarKFull + st), ((s < n) + (s > 0)) * Lay::kKVBytes);
-            if (s < n) issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKFull + st), s, false);
-            if (s > 0) issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarKFull + st), s - 1, true);
+            if (leader) mbar_arrive_expect_tx(bar(kBarKvFull + st), ((s < n) + (s > 0)) * Lay::kKVBytes);
+            if (s < n) issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKvFull + st), s, false);
+            if (s > 0) issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarKvFull + st), s - 1, true);
             ++nk;
           }
         }
-        if (kSparse && ok && prev >= 0) ok = load_v(prev);
         if (!ok) break;
       }
       // no copy may land after the CTA is gone: wait for the last armed phase of each barrier
       if (nq) mbar_drain(bar(kBarQFull), (nq - 1) & 1);
       for (uint32_t st = 0; st < 2; ++st) {
-        const uint32_t ck = (nk + 1 - st) / 2, cv = (nv + 1 - st) / 2;  // loads issued into stage st
-        if (ck) mbar_drain(bar(kBarKFull + st), (ck - 1) & 1);
-        if (cv) mbar_drain(bar(kBarVFull + st), (cv - 1) & 1);
+        const uint32_t c = (nk + 1 - st) / 2;  // steps loaded into slot st
+        if (c) mbar_drain(bar(kBarKvFull + st), (c - 1) & 1);
       }
     }
   } else if (warp == 1) {
@@ -478,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0);  // Q K^T: both K-major
       constexpr uint32_t idO = idesc_bf16_f32(BM, D, 1);   // P V: V is MN-major (d contiguous)
-      uint32_t nq = 0, nk = 0, nv = 0;
+      uint32_t nq = 0, nk = 0;                             // nk: K/V ring steps consumed
       uint32_t np[2] = {0, 0};                             // P_X buffers consumed so far
       uint32_t si[2] = {0, 0};                             // S_X issued (dense d = 64)
       // Descriptor bases, built once. The start-address field (bits 0-13, in
@@ -556,13 +547,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int n = max(x.n[0], x.n[1]);
           int done0 = 0, done1 = 0;          // P V products issued per tile
           bool had0 = false, had1 = false;    // tile kept the previous union block
-          bool first = true;
           BitWalk walk(mw, 3, n);
           for (int j = walk.next(); j >= 0; j = walk.next()) {
             const bool a0 = walk.kept(0), a1 = walk.kept(1);
-            const uint32_t kst = nk & 1, vst = nv & 1;
-            if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
-                (!first && !mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns))) {
+            const uint32_t kst = nk & 1, vst = kst;  // K of block j, V of the previous kept block
+            if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -579,18 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (a1) issue_s(1, kst);
             had0 = a0;
             had1 = a1;
-            mma_commit(bar(kBarKEmpty + kst));
+            mma_commit(bar(kBarKvEmpty + kst));
             ++nk;
-            if (!first) {
-              mma_commit(bar(kBarVEmpty + vst));
-              ++nv;
-            }
             if (j == last) mma_commit(bar(kBarQEmpty));
-            first = false;
           }
           if (!ok) break;
-          const uint32_t vst = nv & 1;
-          if (!mbar_wait(bar(kBarVFull + vst), (nv >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          const uint32_t vst = nk & 1;  // V of the last kept block alone
+          if (!mbar_wait(bar(kBarKvFull + vst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (had0) {
             if (!issue_pv(0, vst, done0 > 0)) break;
@@ -600,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!issue_pv(1, vst, done1 > 0)) break;
             mma_commit(bar(kBarOFull + 1));
           }
-          mma_commit(bar(kBarVEmpty + vst));
-          ++nv;
+          mma_commit(bar(kBarKvEmpty + vst));
+          ++nk;
           mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
           ++nm;
           continue;
@@ -631,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // step j: S_A(j), S_B(j) (j < n) and O_t += P_t(j-1) V_{j-1} (j > 0), K_j and
             // V_{j-1} in slot nk mod 2 under one barrier pair
             const uint32_t st = nk & 1;
-            if (!mbar_wait(bar(kBarKFull + st), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
+            if (!mbar_wait(bar(kBarKvFull + st), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
                 (j < nA && !early_s(0, st)) || (j < nB && !early_s(1, st))) {
               ok = false;
               break;
@@ -644,7 +628,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
               }
             }
-            mma_commit(bar(kBarKEmpty + st));
+            mma_commit(bar(kBarKvEmpty + st));
             ++nk;
           }
           continue;
@@ -652,17 +636,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // j = 0
         {
           const uint32_t kst = nk & 1;
-          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           issue_s(0, kst);
           if (nB > 0) issue_s(1, kst);
-          mma_commit(bar(kBarKEmpty + kst));
+          mma_commit(bar(kBarKvEmpty + kst));
           ++nk;
           if (n == 1) mma_commit(bar(kBarQEmpty));
         }
         for (int j = 1; ok && j < n; ++j) {
           const uint32_t kst = nk & 1, vst = kst;  // K_j and V_{j-1}: one slot, one barrier
-          if (!mbar_wait(bar(kBarKFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) {
+          if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -677,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j - 1 == nB - 1) mma_commit(bar(kBarOFull + 1));
           }
           if (j < nB) issue_s(1, kst);
-          mma_commit(bar(kBarKEmpty + kst));
+          mma_commit(bar(kBarKvEmpty + kst));
           ++nk;
           if (j == n - 1) mma_commit(bar(kBarQEmpty));
         }
@@ -685,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // tail: the last P V of each tile
         {
           const uint32_t vst = nk & 1;  // V_{n-1} alone in the item's last slot
-          if (!mbar_wait(bar(kBarKFull + vst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          if (!mbar_wait(bar(kBarKvFull + vst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (n - 1 < nA) {
             if (!issue_pv(0, vst, n - 1 > 0)) break;
@@ -695,7 +679,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!issue_pv(1, vst, n - 1 > 0)) break;
             mma_commit(bar(kBarOFull + 1));
           }
-          mma_commit(bar(kBarKEmpty + vst));
+          mma_commit(bar(kBarKvEmpty + vst));
           ++nk;
         }
       }
