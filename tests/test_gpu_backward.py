@@ -49,6 +49,26 @@ def test_backward_parity(fa, B, N, Hq, Hkv, d, causal):
         assert mean <= 4e-3 * max(rmean, 1e-3), f"{name}: mean err {mean:.3e} (ref mean {rmean:.3f})"
 
 
+@pytest.mark.parametrize("scale,d", [(-0.1, 128), (0.3, 64)])
+def test_backward_parity_other_scales(fa, scale, d):
+    """dQ = scale dS K, dK = scale dS^T Q with a negative and a large scale (B=2, N=300,
+    GQA 4:2, causal)."""
+    x = inputs.prefill_dense(4500 + d, 2, 300, 4, 2, d, True, scale=scale)
+    g = torch.Generator("cpu").manual_seed(4600 + d)
+    do = torch.randn((2, 300, 4, d), generator=g).to(torch.bfloat16)
+    q, k, v, dog = x.q.cuda(), x.k.cuda(), x.v.cuda(), do.cuda()
+    o, lse = fa.fwd(q, k, v, causal=True, scale=scale)
+    dq, dk, dv = fa.bwd(q, k, v, o, lse, dog, causal=True, scale=scale)
+    assert fa.debug_read_status() == 0
+    rq, rk, rv = orc.attn_bwd(x.q, x.k, x.v, do, scale, True)
+    for name, a, r in (("dq", dq, rq), ("dk", dk, rk), ("dv", dv, rv)):
+        mx, mean, rmax, rmean = _grad_err(a, r)
+        print(name, f"max {mx:.3e} mean {mean:.3e} | ref max {rmax:.3f} mean {rmean:.3f}")
+        assert np.all(np.isfinite(as_np(a)))
+        assert mx <= 2e-2 * max(1.0, rmax), f"{name}: max err {mx:.3e} (ref max {rmax:.3f})"
+        assert mean <= 4e-3 * max(rmean, 1e-3), f"{name}: mean err {mean:.3e} (ref mean {rmean:.3f})"
+
+
 def test_backward_full_size_every_item(fa):
     """The bench's workload (causal MHA B=4 H=32 N=4096 d=128) in the launch the bench
     times, on NaN-filled gradient buffers: every entry must be written, and the

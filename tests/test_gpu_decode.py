@@ -91,6 +91,17 @@ def test_other_page_sizes_and_head_dims(fa, page_size, d):
     check(o, lse, o_ref, lse_ref, what=f"page {page_size} d {d}")
 
 
+@pytest.mark.parametrize("scale", [-0.12, 0.35])
+def test_other_scales(fa, scale):
+    """A negative and a large scale (any finite value is accepted), 3 sequences up to
+    1000 tokens, GQA 8:2, d = 128, 16-token pages, 5 splits."""
+    x = inputs.decode_paged(60, 3, 8, 2, 128, 16, (1, 900), 1000, spare_pages=3, scale=scale)
+    o_ref, lse_ref = orc.decode_paged(x.q, x.kcache, x.vcache, x.block_table, x.seqlens, x.scale)
+    o, lse, _, st = _decode(fa, x, 5)
+    assert st == 0
+    check(o, lse, o_ref, lse_ref, what=f"decode scale {scale}")
+
+
 def test_zero_length_sequence(fa):
     x = inputs.decode_paged(50, 3, 4, 1, 64, 16, None, 256, spare_pages=1, lengths=[17, 1, 200])
     dev = list(_dev(x))

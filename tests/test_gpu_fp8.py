@@ -89,6 +89,21 @@ def test_fp8_parity(fa, B, N, Hq, Hkv, causal):
     _check_fp8(og, lg, o_ref, lse_ref, x, rows, f"fp8 {B, N, Hq, Hkv, causal}")
 
 
+@pytest.mark.parametrize("scale", [-0.1, 0.25])
+def test_fp8_parity_other_scales(fa, scale):
+    """A negative and a large scale (folded with the q and k descales into the exponent
+    scale), B=2 N=300 GQA 4:2 causal."""
+    x = inputs.prefill_fp8(6500 + int(100 * scale), 2, 300, 4, 2, 128, True, scale=scale)
+    o, lse = fa.fwd_fp8(x.q8.cuda(), x.k8.cuda(), x.v8.cuda(), x.q_descale, x.k_descale, x.v_descale,
+                        causal=True, scale=x.scale)
+    assert fa.debug_read_status() == 0
+    rows = _all_rows(2, 4, 300)
+    o_ref, lse_ref = orc.attn_fwd_fp8(x.q8, x.k8, x.v8, x.q_descale, x.k_descale, x.v_descale, x.scale, True,
+                                      rows=rows)
+    og, lg = _flat(o, lse, rows)
+    _check_fp8(og, lg, o_ref, lse_ref, x, rows, f"fp8 scale {scale}")
+
+
 def test_fp8_large_every_item(fa):
     """Causal MHA B=4, H=32, N=4096, d=128 in E4M3, on NaN-filled outputs: every row
     written, both edge rows of every (sequence, head, 128-row tile) and random rows

@@ -50,6 +50,18 @@ def test_masked_parity(fa, B, N, Hq, Hkv, d, causal, Bm, Hm):
     assert np.all(og[:, 3] == 0) and np.all(np.isneginf(as_np(lse)[:, :, 3]))   # the fully masked row
 
 
+@pytest.mark.parametrize("scale,d", [(-0.2, 128), (0.3, 64)])
+def test_masked_parity_other_scales(fa, scale, d):
+    """The mask is added to the scaled scores, so a negative scale changes which keys
+    dominate but not the max rule; B=2 N=300 GQA 4:2 causal, one mask per (b, h)."""
+    x = inputs.prefill_dense(5500 + d, 2, 300, 4, 2, d, True, scale=scale)
+    m = _mask(5600 + d, 2, 4, 300)
+    o, lse = fa.fwd_masked(x.q.cuda(), x.k.cuda(), x.v.cuda(), m.cuda(), causal=True, scale=scale)
+    assert fa.debug_read_status() == 0
+    o_ref, lse_ref = orc.attn_fwd_masked(x.q, x.k, x.v, scale, True, m[..., :300].float().numpy())
+    check(o, lse, o_ref, lse_ref, what=f"masked scale {scale} d {d}")
+
+
 def test_lower_triangle_mask_equals_causal(fa):
     x = inputs.prefill_dense(5200, 1, 384, 4, 4, 128, True)
     N = 384

@@ -90,6 +90,28 @@ def test_dense_parity(fa, B, N, Hq, Hkv, d, causal):
     check(o, lse, o_ref, lse_ref, what=f"dense {B,N,Hq,Hkv,d,causal}")
 
 
+@pytest.mark.parametrize("scale", [-0.2, 0.02, 0.4])
+@pytest.mark.parametrize("d,causal", [(64, True), (64, False), (128, True), (128, False)])
+def test_dense_parity_other_scales(fa, scale, d, causal):
+    """Any finite scale is accepted ('scale multiplies Q K^T'): a negative one (the row
+    maximum of the scaled scores is then the minimum of Q K^T, and masked keys go to
+    +inf before scaling), a small one (nearly uniform weights) and a large one (peaked
+    weights), at both head dimensions (d = 64 runs the separate-P schedule), B=2 N=300
+    (tiles plus a ragged tail), GQA 4:2."""
+    x = inputs.prefill_dense(3000 + d + int(100 * scale), 2, 300, 4, 2, d, causal, scale=scale)
+    o, lse = _run(fa, x)
+    o_ref, lse_ref = _ref(x)
+    check(o, lse, o_ref, lse_ref, what=f"dense scale {scale} d {d} causal {causal}")
+
+
+@pytest.mark.parametrize("scale", [-0.15, 0.3])
+def test_dense_parity_other_scales_fp32(fa, scale):
+    x = inputs.prefill_dense(3500 + int(100 * scale), 2, 300, 4, 2, 64, True, dtype=torch.float32, scale=scale)
+    o, lse = _run(fa, x, fp32=True)
+    o_ref, lse_ref = _ref(x, fp32=True)
+    check(o, lse, o_ref, lse_ref, fp32=True, what=f"fp32 scale {scale}")
+
+
 @pytest.mark.parametrize("B,N,Hq,Hkv,d,causal", CASES[:5])
 def test_dense_parity_fp32(fa, B, N, Hq, Hkv, d, causal):
     x = inputs.prefill_dense(2000 + N + d, B, N, Hq, Hkv, d, causal)
