@@ -582,7 +582,7 @@ struct DqLayout {
   static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 enum : int {
-  kQFull = 0, kQEmpty = 1, kKFull = 2, kKEmpty = 5, kVFull = 8, kVEmpty = 10, kQSFull = 12, kQSFree = 13,
+  kQFull = 0, kQEmpty = 1, kQKvFull = 2, kKEmpty = 5, kVEmpty = 10, kQSFull = 12,
   kQDpFull = 14, kQDpFree = 15, kQDsFull = 16, kQAccFull = 17, kQAccEmpty = 18, kQMmaDone = 19
 };
 // dQ pass: dS of key tile n goes to TMEM columns [kColDs + 64 (n & 1), +64) (bf16 pairs;
@@ -605,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
-      mbar_init(bar(i), (i == kQSFree || i == kQDpFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
+      mbar_init(bar(i), (i == kQDpFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
     mbar_init(bar(Lay::kBarStall), 1);
     *abort = 0;
     fence_mbar_init();
@@ -653,44 +653,40 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
         const int jn = p.causal ? i + 1 : nt, hkv = h / G;
         for (int j = 0; j < jn; ++j) {
+          // K_j (stage j mod 3) and V_j (stage j mod 2) land on one barrier, QKvFull j mod 2:
+          // the MMA issuer waits once for both (S_j comes before dP_j). Two slots suffice:
+          // step j + 2 is armed only after V_j's stage is free, i.e. after dP_j, which the
+          // issuer started after its wait for step j.
           const uint32_t ks = nk % 3, vs = nv & 1;
-          if (!mbar_wait(bar(kKEmpty + ks), ((nk / 3) & 1) ^ 1, abort, p.status, p.wait_ns)) {
+          if (!mbar_wait(bar(kKEmpty + ks), ((nk / 3) & 1) ^ 1, abort, p.status, p.wait_ns) ||
+              !mbar_wait(bar(kVEmpty + vs), ((nv >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(kKFull + ks), Lay::kTile);
-          load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kKFull + ks), hkv, b * p.N + j * BT, pol_kv);
+          mbar_arrive_expect_tx(bar(kQKvFull + vs), 2 * Lay::kTile);
+          load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kQKvFull + vs), hkv, b * p.N + j * BT, pol_kv);
+          load_tile<D>(sb + Lay::kOffV + vs * Lay::kTile, &tv, bar(kQKvFull + vs), hkv, b * p.N + j * BT, pol_kv);
           ++nk;
-          if (!mbar_wait(bar(kVEmpty + vs), ((nv >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(kVFull + vs), Lay::kTile);
-          load_tile<D>(sb + Lay::kOffV + vs * Lay::kTile, &tv, bar(kVFull + vs), hkv, b * p.N + j * BT, pol_kv);
           ++nv;
         }
       }
       // wait for the last load into each buffer before the CTA may exit
       if (nq) mbar_drain(bar(kQFull), (nq - 1) & 1);
-      for (uint32_t st = 0; st < 3; ++st) {
-        const uint32_t c = (nk + 2 - st) / 3;
-        if (c) mbar_drain(bar(kKFull + st), (c - 1) & 1);
-      }
       for (uint32_t st = 0; st < 2; ++st) {
-        const uint32_t c = (nv + 1 - st) / 2;
-        if (c) mbar_drain(bar(kVFull + st), (c - 1) & 1);
+        const uint32_t c = (nv + 1 - st) / 2;  // steps armed on slot st
+        if (c) mbar_drain(bar(kQKvFull + st), (c - 1) & 1);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // per key tile j: S_j = Q K_j^T and dP_j = dO V_j^T; S_{j+1} as soon as the
-    // element-wise warps have read S_j, dP_{j+1} as soon as they have read dP_j,
-    // then dQ += dS_j K_j once dS_j is written. dS alternates between two TMEM
+    // per key tile j: S_j = Q K_j^T and dP_j = dO V_j^T; S_{j+1} and dP_{j+1} as soon
+    // as the element-wise warps have read S_j and dP_j (one signal for both), then
+    // dQ += dS_j K_j once dS_j is written. dS alternates between two TMEM
     // buffers: dS_{n+2} is written only after dP_{n+2} completes, which was issued
     // after dQ += dS_n K_n, so that product has finished reading buffer n & 1.
     if (lane == 0) {
       // n counts key tiles over all items: K_n in K stage n % 3, V_n in V stage n % 2
-      uint32_t nq = 0, n = 0, nfree = 0, ndpf = 0, nacc = 0;
+      uint32_t nq = 0, n = 0, ndpf = 0, nacc = 0;
       const uint64_t qd = smem_desc_sw128(sb + Lay::kOffQ, 16, 1024);
       const uint64_t dod = smem_desc_sw128(sb + Lay::kOffDO, 16, 1024);
       const uint32_t tS = tmem + kColS, tDP = tmem + kColDP, tDQ = tmem + kColAcc;
@@ -698,16 +694,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto k_addr = [&](uint32_t t) -> uint32_t { return sb + Lay::kOffK + (t % 3) * Lay::kTile; };
       auto v_addr = [&](uint32_t t) -> uint32_t { return sb + Lay::kOffV + (t & 1) * Lay::kTile; };
       // S_t = Q K_t^T
-      auto issue_s = [&](uint32_t t) -> bool {
-        if (!mbar_wait(bar(kKFull + t % 3), (t / 3) & 1, abort, p.status, p.wait_ns)) return false;
+      auto issue_s = [&](uint32_t t) -> bool {  // K_t and V_t have landed after this wait
+        if (!mbar_wait(bar(kQKvFull + (t & 1)), (t >> 1) & 1, abort, p.status, p.wait_ns)) return false;
         tc_fence_after();
         issue_kk<D>(tS, qd, smem_desc_sw128(k_addr(t), 16, 1024));
         mma_commit(bar(kQSFull));
         return true;
       };
       // dP_t = dO V_t^T, then V_t's stage is free
-      auto issue_dp = [&](uint32_t t) -> bool {
-        if (!mbar_wait(bar(kVFull + (t & 1)), (t >> 1) & 1, abort, p.status, p.wait_ns)) return false;
+      auto issue_dp = [&](uint32_t t) -> bool {  // after issue_s(t), whose wait covers V_t
         tc_fence_after();
         issue_kk<D>(tDP, dod, smem_desc_sw128(v_addr(t), 16, 1024));
         mma_commit(bar(kQDpFull));
@@ -722,13 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nq;
         if (!issue_s(n) || !issue_dp(n)) break;
         for (int j = 0; j < jn; ++j, ++n) {
-          if (j + 1 < jn) {
-            if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, p.wait_ns) || !issue_s(n + 1)) {
-              ok = false;
-              break;
-            }
-            ++nfree;
-            if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns) || !issue_dp(n + 1)) {
+          if (j + 1 < jn) {  // S_n and dP_n both read: the next two products may overwrite them
+            if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns) || !issue_s(n + 1) ||
+                !issue_dp(n + 1)) {
               ok = false;
               break;
             }
@@ -748,10 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // the item's last S and dP were read before its last dS was written
-        if (!mbar_wait(bar(kQSFree), nfree & 1, abort, p.status, p.wait_ns) ||
-            !mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns))
-          break;
-        ++nfree;
+        if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns)) break;
         ++ndpf;
         mma_commit(bar(kQEmpty));
         mma_commit(bar(kQAccFull));
@@ -794,9 +782,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
           uint32_t u[64];
           tmem_ld64(s_col, u);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kQSFree));  // S may be overwritten by the next tile's product
           // visible keys of this tile: column c < lim
           const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - j * BT - cb;
 #pragma unroll
@@ -817,7 +802,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld64(dp_col, a);
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(kQDpFree));  // dP may be overwritten by the next tile's product
+          // S and dP may be overwritten by the next tile's products (one signal for both: one
+          // wait fewer for the MMA issuer)
+          if (lane == 0) mbar_arrive(bar(kQDpFree));
           // dS = P o (dP - D) as bf16 pairs
           uint32_t w[32];
 #pragma unroll
