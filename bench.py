@@ -347,12 +347,10 @@ def fp8_leg(fattn, pre, flush, stream, peaks, dev):
     B, N, Hq, d = pre.q.shape
     x = inputs.prefill_fp8(1, B, N, Hq, pre.hkv, d, True)
     q8, k8, v8 = x.q8.to(dev), x.k8.to(dev), x.v8.to(dev)
-    ws = torch.empty(int(fattn.load_library().fattn_fwd_fp8_workspace_size(B, pre.hkv, N, d)), dtype=torch.uint8,
-                     device=dev)
     o = torch.empty(q8.shape, dtype=torch.bfloat16, device=dev)
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
     t = _time_launches(lambda: fattn.fwd_fp8(q8, k8, v8, x.q_descale, x.k_descale, x.v_descale, causal=True,
-                                             scale=x.scale, out=o, lse=lse, workspace=ws), flush, stream)
+                                             scale=x.scale, out=o, lse=lse), flush, stream)
     tf = x.flops() / (t * 1e-3) / 1e12
     peak8, src8 = fp8_gemm_peak(dev)
     if peak8 is None:

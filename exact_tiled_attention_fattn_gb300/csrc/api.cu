@@ -277,16 +277,9 @@ extern "C" fattn_status fattn_fwd_paged(const void* q, const void* kcache, const
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-extern "C" size_t fattn_fwd_fp8_workspace_size(int B, int Hkv, int N, int d) {
-  if (B <= 0 || Hkv <= 0 || N <= 0 || d <= 0) return 0;
-  const size_t npad = ((size_t)N + 127) / 128 * 128;
-  return align256((size_t)B * Hkv * d * npad);
-}
-
 extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                                       int Hkv, int N, int d, int causal, float scale, float q_descale,
-                                      float k_descale, float v_descale, void* workspace, size_t workspace_bytes,
-                                      cudaStream_t stream) {
+                                      float k_descale, float v_descale, cudaStream_t stream) {
   if (B < 0 || N < 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return FATTN_ERR_INVALID_ARG;
   if (B == 0 || N == 0) return FATTN_OK;
   if (!q || !k || !v || !o) return FATTN_ERR_INVALID_ARG;
@@ -298,15 +291,11 @@ extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* 
   if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)) return FATTN_ERR_INVALID_ARG;
   if (d != 128) return FATTN_ERR_UNSUPPORTED;
   const long long rows = (long long)B * N;
-  const long long npad = ((long long)N + 127) / 128 * 128;
-  if (rows > 0x7fffffffLL || npad > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
-  const size_t need = fattn_fwd_fp8_workspace_size(B, Hkv, N, d);
-  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u))
-    return FATTN_ERR_WORKSPACE;
+  if (rows > 0x7fffffffLL) return FATTN_ERR_UNSUPPORTED;
 
   int err = 0;
   PrefillParams p{};
-  p.q = q; p.k = k; p.v = workspace; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
+  p.q = q; p.k = k; p.v = v; p.o = o; p.lse = lse; p.cu_seqlens = nullptr;
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.total_rows = (int)rows;
   p.causal = causal ? 1 : 0;
   p.scale = scale * q_descale * k_descale;  // S = scale (q_descale Q8)(k_descale K8)^T
@@ -316,13 +305,10 @@ extern "C" fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* 
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);
-  uint8_t* vt = static_cast<uint8_t*>(workspace);
-  if (launch_fp8_transpose_v(static_cast<const uint8_t*>(v), vt, B, N, Hkv, d, (int)npad, stream) != cudaSuccess)
-    return FATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, to;
   if (!encode_u8_map(&tq, q, d, Hq, rows, (uint64_t)d, (uint64_t)Hq * d, 128, 1, 128) ||
       !encode_u8_map(&tk, k, d, Hkv, rows, (uint64_t)d, (uint64_t)Hkv * d, 128, 1, 128) ||
-      !encode_u8_map(&tv, vt, npad, d, (uint64_t)B * Hkv, (uint64_t)npad, (uint64_t)npad * d, 128, 128, 1) ||
+      !encode_u8_map(&tv, v, d, Hkv, rows, (uint64_t)d, (uint64_t)Hkv * d, 128, 1, 128) ||
       !encode_rows_map(&to, o, (int)rows, Hq, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();

@@ -42,8 +42,8 @@ struct PrefillParams {
   const void* mask;           // nullptr = none
   long long mask_sb, mask_sh;
   int mask_ld;
-  // FP8 variant only: E4M3 q and k ([rows, H, d]), v transposed to [B * Hkv, d, Npad]
-  // (the tv tensor map); scale already holds scale * q_descale * k_descale
+  // FP8 variant only: E4M3 q, k and v ([rows, H, d]); scale already holds
+  // scale * q_descale * k_descale
   int fp8;
   float v_descale;
   // bounded pipeline waits: each mbarrier wait gives up after wait_ns; debug_stall != 0
@@ -52,10 +52,6 @@ struct PrefillParams {
   unsigned long long wait_ns;
   int debug_stall;
 };
-
-// V [B, N, Hkv, d] (E4M3 bytes) -> V^T [B * Hkv, d, Npad], zero past N (d = 128).
-cudaError_t launch_fp8_transpose_v(const uint8_t* v, uint8_t* vt, int B, int N, int Hkv, int d, int Npad,
-                                   cudaStream_t stream);
 
 // Longest mask row (blocks) the block-sparse kernel holds in shared memory.
 constexpr int kSparseMaxBlocks = 2048;

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kSparse = kMode == kModeSparse;  // fixed block mask, zero blocks skipped
   constexpr bool kPaged = kMode == kModePaged;    // K/V through a block table
   constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
-  constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V^T; P in E4M3 through shared memory
+  constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V; P in E4M3 through shared memory
   static_assert(!kFp8 || D == 128, "FP8 tiles are 128 one-byte columns: one 128-byte swizzle span");
   constexpr int kChunks = kFp8 ? 1 : D / 64;      // 128-byte boxes per tile row
   using Lay = TcLayout<D, kMode>;
@@ -385,12 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // box beyond the pool, which the copy fills with zeros. The boxes stack into the
         // same swizzled layout as one 128-row box (page_size is a multiple of 8 rows).
         auto issue_kv = [&](const CUtensorMap* map, uint32_t dst, uint32_t full, int j, bool is_v) {
-          if constexpr (kFp8) {
-            if (is_v) {  // V^T tile: head-dim rows, 128 keys per row, from the transposed copy
-              tma_load_3d(dst, map, full, j * BN, 0, x.b * p.Hkv + hkv, pol_kv);
-              return;
-            }
-          }
+          (void)is_v;
           if constexpr (kPaged) {
             const int P = p.page_size, per = BN / P;  // per <= 8 (page_size >= 16)
             const int i = lane;                       // this lane's page of the tile
@@ -479,14 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t qd1 = smem_desc_sw128(sb + Lay::kOffQ + Lay::kQBytes, 16, 1024);
       const uint64_t kd0 = smem_desc_sw128(sb + Lay::kOffK, 16, 1024);
       const uint64_t kd1 = smem_desc_sw128(sb + Lay::kOffK + Lay::kKVBytes, 16, 1024);
-      // V: MN-major (d contiguous) for bf16; the FP8 variant holds V^T, K-major
-      const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, kFp8 ? 16 : BN * 128, 1024);
-      const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, kFp8 ? 16 : BN * 128, 1024);
+      // V: MN-major (d contiguous, 128-byte column blocks BN * 128 bytes apart; the FP8
+      // tile's d = 128 bytes is a single block)
+      const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, BN * 128, 1024);
+      const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, BN * 128, 1024);
       auto issue_s = [&](int t, uint32_t kst) {
         const uint32_t d_tmem = tmem + Lay::col_s(t);
         const uint64_t a0 = t ? qd1 : qd0, b0 = kst ? kd1 : kd0;
         if constexpr (kFp8) {  // K = 32 one-byte elements (32 bytes) per instruction
-          constexpr uint32_t idS8 = idesc_e4m3_f32(BM, BN);
+          constexpr uint32_t idS8 = idesc_e4m3_f32(BM, BN, 0);
           mma_ss_e4m3<false>(d_tmem, a0, b0, idS8);
 #pragma unroll
           for (int ks = 1; ks < D / 32; ++ks) mma_ss_e4m3<true>(d_tmem, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 2), idS8);
@@ -508,12 +504,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t p_tmem = tmem + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t)), o_tmem = tmem + Lay::col_o(t);
         const uint64_t b0 = vst ? vd1 : vd0;
-        if constexpr (kFp8) {  // O += P V with P (E4M3, shared memory) and V^T both K-major
-          constexpr uint32_t idO8 = idesc_e4m3_f32(BM, D);
+        if constexpr (kFp8) {  // O += P V with P (E4M3, shared memory, K-major) and V (MN-major)
+          constexpr uint32_t idO8 = idesc_e4m3_f32(BM, D, 1);
           const uint64_t a0 = smem_desc_sw128(sb + Lay::kOffP + t * Lay::kPBytes, 16, 1024);
           mma_ss_e4m3_p(o_tmem, a0, b0, idO8, acc ? 1u : 0u);
+          // K = 32 keys per instruction: P advances 32 bytes along its rows, V 32 rows of 128 bytes
 #pragma unroll
-          for (int ks = 1; ks < BN / 32; ++ks) mma_ss_e4m3<true>(o_tmem, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 2), idO8);
+          for (int ks = 1; ks < BN / 32; ++ks)
+            mma_ss_e4m3<true>(o_tmem, a0 + (uint64_t)(ks * 2), b0 + (uint64_t)(ks * 32 * 128 / 16), idO8);
           return true;
         }
         mma_ts(o_tmem, p_tmem, b0, idO, acc ? 1u : 0u);
@@ -857,12 +855,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           // exponent), one packed FMA per column pair, 32 columns at a time so each
           // mask word dies as its scores arrive; keys past the visible limit -inf
           // (their p is 0 below)
+          uint32_t u[BN];
+          tmem_ld128(s_col, u);  // one wait for all 128 scores
           cp_async_wait_all();
           __syncwarp();  // the warp's copies of the second half have landed
 #pragma unroll
           for (int q32 = 0; q32 < BN / 32; ++q32) {
-            uint32_t u[32];
-            tmem_ld32(s_col + 32 * q32, u);
             uint4 gq[4];  // this 32-column group's mask entries
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
@@ -876,7 +874,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint4& g = gq[e >> 3];
               const uint32_t w = ((c & 7) >> 1) == 0 ? g.x : ((c & 7) >> 1) == 1 ? g.y : ((c & 7) >> 1) == 2 ? g.z : g.w;
               float t0, t1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), scale2,
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(u[c]), __uint_as_float(u[c + 1])), scale2,
                                f2_pack(bf16_lo(w), bf16_hi(w))), t0, t1);
               s[c] = t0;
               s[c + 1] = t1;

@@ -227,9 +227,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, int b_mn) {
 }
 
 // Instruction descriptor of kind::f8f6f4 with E4M3 A and B (format code 0),
-// fp32 accumulator, both K-major, shape M x N.
-__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+// fp32 accumulator, A K-major, B K-major (b_mn = 0) or MN-major (1), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N, int b_mn) {
   return (1u << 4)                          // D format: f32
+         | ((uint32_t)b_mn << 16)           // B major-ness
          | ((uint32_t)(N >> 3) << 17)       // N / 8
          | ((uint32_t)(M >> 4) << 24);      // M / 16
 }

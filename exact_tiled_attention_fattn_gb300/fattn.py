@@ -34,8 +34,7 @@ SIGNATURES = {
     "fattn_fwd_block_sparse": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _i, _vp]),
     "fattn_fwd_masked": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, ctypes.c_longlong,
                               ctypes.c_longlong, _i, _vp]),
-    "fattn_fwd_fp8_workspace_size": (_sz, [_i, _i, _i, _i]),
-    "fattn_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _f, _f, _f, _vp, _sz, _vp]),
+    "fattn_fwd_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _f, _f, _f, _vp]),
     "fattn_fwd_paged": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _i, _i, _i, _f,
                              _vp]),
     "fattn_bwd_workspace_size": (_sz, [_i, _i, _i]),
@@ -262,11 +261,11 @@ def fwd_masked(q, k, v, mask, causal: bool = False, scale: float | None = None, 
 
 
 def fwd_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float, causal: bool = False,
-            scale: float | None = None, out=None, lse=None, want_lse: bool = True, workspace=None, stream=None):
+            scale: float | None = None, out=None, lse=None, want_lse: bool = True, stream=None):
     """FP8 prefill. q8 [B,N,Hq,d], k8/v8 [B,N,Hkv,d] E4M3 (torch.float8_e4m3fn or uint8 codes),
     d = 128; the inputs are descale * e4m3. Returns (O bf16 [B,N,Hq,d], lse [B,Hq,N])."""
     lib = load_library()
-    _need_cuda(q8, k8, v8, out, lse, workspace)
+    _need_cuda(q8, k8, v8, out, lse)
     for t in (q8, k8, v8):
         if t.dtype not in (torch.uint8, torch.float8_e4m3fn):
             raise TypeError("fp8 prefill takes E4M3 tensors (float8_e4m3fn or uint8 codes)")
@@ -283,12 +282,8 @@ def fwd_fp8(q8, k8, v8, q_descale: float, k_descale: float, v_descale: float, ca
         out = torch.empty(q8.shape, dtype=torch.bfloat16, device=q8.device)
     if lse is None and want_lse:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q8.device)
-    need = int(lib.fattn_fwd_fp8_workspace_size(B, k8.shape[2], N, d))
-    if workspace is None:
-        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q8.device)
     st = lib.fattn_fwd_fp8(_ptr(q8), _ptr(k8), _ptr(v8), _ptr(out), _ptr(lse), B, Hq, k8.shape[2], N, d,
                            1 if causal else 0, float(scale), float(q_descale), float(k_descale), float(v_descale),
-                           _ptr(workspace), workspace.numel() * workspace.element_size(),
                            ctypes.c_void_p(_stream_handle(stream)))
     _check("fattn_fwd_fp8", st)
     return out, lse

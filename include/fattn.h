@@ -141,18 +141,15 @@ fattn_status fattn_fwd_masked(const void* q, const void* k, const void* v, void*
  * Dense layout: q [B, N, Hq, d], k, v [B, N, Hkv, d] as E4M3 bytes ('fn'
  * variant: no infinities); o [B, N, Hq, d] bf16; lse [B, Hq, N] fp32 (may be
  * NULL). Both products run on E4M3 operands with fp32 accumulation; P is
- * rounded to E4M3 for P V (the row sums use the unrounded P).
- * workspace: DEVICE, >= fattn_fwd_fp8_workspace_size(B, Hkv, N, d) bytes,
- *   256-byte aligned: holds V transposed ([B * Hkv, d, N rounded up to 128]).
+ * rounded to E4M3 for P V (the row sums use the unrounded P). V is read in
+ * place (no copy, no workspace).
  * Errors: INVALID_ARG (NULL or misaligned pointers, negative sizes,
  *   Hq % Hkv != 0, a descale that is not finite and positive), UNSUPPORTED
- *   (d != 128, B * N >= 2^31), WORKSPACE (missing, small or misaligned).
+ *   (d != 128, B * N >= 2^31).
  */
-size_t fattn_fwd_fp8_workspace_size(int B, int Hkv, int N, int d);
 fattn_status fattn_fwd_fp8(const void* q, const void* k, const void* v, void* o, float* lse,
                            int B, int Hq, int Hkv, int N, int d, int causal, float scale,
-                           float q_descale, float k_descale, float v_descale,
-                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+                           float q_descale, float k_descale, float v_descale, cudaStream_t stream);
 
 /*
  * fattn_fwd_paged — prefill of query chunks against a paged KV cache

@@ -33,7 +33,7 @@ def test_every_declared_symbol_is_exported(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == {"fattn_fwd", "fattn_fwd_block_sparse", "fattn_fwd_masked", "fattn_fwd_fp8",
-                          "fattn_fwd_fp8_workspace_size", "fattn_fwd_paged", "fattn_bwd",
+                          "fattn_fwd_paged", "fattn_bwd",
                           "fattn_bwd_workspace_size", "fattn_decode_workspace_size",
                           "fattn_decode_paged",
                           "fattn_decode_paged_static", "fattn_merge_partials", "fattn_status_string",
@@ -194,14 +194,12 @@ def test_masked_validation(lib):
 
 def test_fp8_validation(lib):
     E = fattn
-    assert lib.fattn_fwd_fp8_workspace_size(2, 4, 300, 128) == 2 * 4 * 128 * 384
-    assert lib.fattn_fwd_fp8_workspace_size(2, 0, 300, 128) == 0
 
     def f(**kw):
         g = lambda n, dflt: kw.get(n, dflt)
         return lib.fattn_fwd_fp8(g("q", A), A, A, A, None, 2, 4, 2, 300, g("d", 128), 1, 0.1, g("qd", 0.01), 0.01,
-                                 0.01, g("ws", A), g("wsb", 1 << 20), None)
+                                 0.01, None)
     assert f(q=None) == E.FATTN_ERR_INVALID_ARG
     assert f(qd=0.0) == E.FATTN_ERR_INVALID_ARG and f(qd=float("nan")) == E.FATTN_ERR_INVALID_ARG
     assert f(d=64) == E.FATTN_ERR_UNSUPPORTED
-    assert f(ws=None) == E.FATTN_ERR_WORKSPACE and f(wsb=1000) == E.FATTN_ERR_WORKSPACE
+
