@@ -220,6 +220,8 @@ extern "C" fattn_status fattn_fwd_masked(const void* q, const void* k, const voi
   p.causal = causal ? 1 : 0; p.scale = scale;
   p.mask_heads = 1;
   p.mask = mask; p.mask_sb = mask_batch_stride; p.mask_sh = mask_head_stride; p.mask_ld = mask_row_stride;
+  p.mask_v8 = (reinterpret_cast<uintptr_t>(mask) & 31u) == 0 && mask_row_stride % 16 == 0 &&
+              mask_batch_stride % 16 == 0 && mask_head_stride % 16 == 0;
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);

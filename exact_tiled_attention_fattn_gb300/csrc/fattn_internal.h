@@ -42,6 +42,8 @@ struct PrefillParams {
   const void* mask;           // nullptr = none
   long long mask_sb, mask_sh;
   int mask_ld;
+  int mask_v8;                // the mask is 32-byte aligned and its strides are multiples of 16
+                              // elements: rows are read with 32-byte loads
   // FP8 variant only: E4M3 q, k and v ([rows, H, d]); scale already holds
   // scale * q_descale * k_descale
   int fp8;

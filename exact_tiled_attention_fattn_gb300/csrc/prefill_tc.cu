@@ -838,8 +838,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             cp_async_16(slot_s + rr * 128 + ((cc ^ (rr & 7)) << 4), src, key0 < rlim ? 16u : 0u);
           }
           cp_async_commit();
+          if (p.mask_v8) {  // 32-byte loads of whole 16-key groups (rows 32-byte aligned)
 #pragma unroll
-          for (int c8 = 0; c8 < BN / 16; ++c8) load_mask(c8);
+            for (int c16 = 0; c16 < BN / 32; ++c16) {
+              if (j * BN + 16 * c16 < lim) {
+                ldg_nc_32b(mrow + j * BN + 16 * c16, mv[2 * c16], mv[2 * c16 + 1]);
+              } else {
+                mv[2 * c16] = make_uint4(0u, 0u, 0u, 0u);
+                mv[2 * c16 + 1] = make_uint4(0u, 0u, 0u, 0u);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int c8 = 0; c8 < BN / 16; ++c8) load_mask(c8);
+          }
         }
         if (!warp_wait(bar(kBarSFull + t), ns & 1, abort, p.status, p.wait_ns)) {
           ok = false;
