@@ -97,13 +97,14 @@ constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8
 static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
 // barrier slots (KvFull / KvEmpty: one pair per K/V ring slot, which holds the K tile
-// and the V tile of one step)
+// and the V tile of one step; room for up to kKvSlotsMax slots)
+constexpr int kKvSlotsMax = 3;
 enum : int {
-  kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 4,
-  kBarSFull = 6, kBarPFull = 8, kBarOFull = 10, kBarMmaDone = 12,
-  kBarMaskFull = 13, kBarMaskEmpty = 13 + kMaskSlots,
+  kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kKvSlotsMax,
+  kBarSFull = 2 + 2 * kKvSlotsMax, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarMmaDone = kBarOFull + 2,
+  kBarMaskFull = kBarMmaDone + 1, kBarMaskEmpty = kBarMaskFull + kMaskSlots,
   // separate P buffers (dense d = 64): S_t read by the softmax, O_t += P_t V completed
-  kBarSFree = 13 + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
+  kBarSFree = kBarMaskFull + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
 };
 
 enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
@@ -120,7 +121,9 @@ struct TcLayout {
   static constexpr int kElem = kFp8 ? 1 : 2;      // bytes per Q/K/V element (E4M3 or bf16)
   static constexpr int kQBytes = BM * D * kElem;  // one Q tile
   static constexpr int kKVBytes = BN * D * kElem;
-  static constexpr int kStages = 2;
+  // K/V ring slots: three for FP8 (its tiles take half the room), two elsewhere
+  static constexpr int kStages = kFp8 ? 3 : 2;
+  static_assert(kStages <= kKvSlotsMax, "K/V ring barriers");
   static constexpr int kOffQ = 0;                 // Q_A then Q_B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
@@ -418,8 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // and V of the previous kept one, then V of the last one alone
           BitWalk walk(mw, 3, n);
           for (int j = walk.next(); ok; j = walk.next()) {
-            const uint32_t st = nk & 1;
-            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
+            const uint32_t st = nk % Lay::kStages;
+            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk / Lay::kStages) & 1) ^ 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -439,8 +442,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           // step, which the tensor core would otherwise wait out (against separate K and V
           // barriers: causal MHA 0.485 -> 0.479 ms, varlen d = 64 0.127 -> 0.119 ms)
           for (int s = 0; ok && s <= n; ++s) {
-            const uint32_t st = nk & 1;
-            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk >> 1) & 1) ^ 1, abort, p.status, p.wait_ns)) {
+            const uint32_t st = nk % Lay::kStages;
+            if (!mbar_wait(bar(kBarKvEmpty + st), ((nk / Lay::kStages) & 1) ^ 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -454,8 +457,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // no copy may land after the CTA is gone: wait for the last armed phase of each barrier
       if (nq) mbar_drain(bar(kBarQFull), (nq - 1) & 1);
-      for (uint32_t st = 0; st < 2; ++st) {
-        const uint32_t c = (nk + 1 - st) / 2;  // steps loaded into slot st
+      for (uint32_t st = 0; st < (uint32_t)Lay::kStages; ++st) {
+        const uint32_t c = nk > st ? (nk - st + Lay::kStages - 1) / Lay::kStages : 0;  // steps loaded into slot st
         if (c) mbar_drain(bar(kBarKvFull + st), (c - 1) & 1);
       }
     }
@@ -472,15 +475,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       // compile-time offset, so issuing an MMA costs no descriptor arithmetic.
       const uint64_t qd0 = smem_desc_sw128(sb + Lay::kOffQ, 16, 1024);
       const uint64_t qd1 = smem_desc_sw128(sb + Lay::kOffQ + Lay::kQBytes, 16, 1024);
+      // ring slot st: with two slots one of two descriptors; with three, the slot-0
+      // descriptor plus st tiles (the start address field counts 16-byte units; every
+      // slot lies below 256 KB, so it never overflows)
       const uint64_t kd0 = smem_desc_sw128(sb + Lay::kOffK, 16, 1024);
       const uint64_t kd1 = smem_desc_sw128(sb + Lay::kOffK + Lay::kKVBytes, 16, 1024);
       // V: MN-major (d contiguous, 128-byte column blocks BN * 128 bytes apart; the FP8
       // tile's d = 128 bytes is a single block)
       const uint64_t vd0 = smem_desc_sw128(sb + Lay::kOffV, BN * 128, 1024);
       const uint64_t vd1 = smem_desc_sw128(sb + Lay::kOffV + Lay::kKVBytes, BN * 128, 1024);
+      auto slot_desc = [&](uint64_t d0, uint64_t d1, uint32_t st) -> uint64_t {
+        if constexpr (Lay::kStages == 2)
+          return st ? d1 : d0;
+        else
+          return d0 + (uint64_t)(st * (Lay::kKVBytes >> 4));
+      };
       auto issue_s = [&](int t, uint32_t kst) {
         const uint32_t d_tmem = tmem + Lay::col_s(t);
-        const uint64_t a0 = t ? qd1 : qd0, b0 = kst ? kd1 : kd0;
+        const uint64_t a0 = t ? qd1 : qd0, b0 = slot_desc(kd0, kd1, kst);
         if constexpr (kFp8) {  // K = 32 one-byte elements (32 bytes) per instruction
           constexpr uint32_t idS8 = idesc_e4m3_f32(BM, BN, 0);
           mma_ss_e4m3<false>(d_tmem, a0, b0, idS8);
@@ -503,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++np[t];
         tc_fence_after();
         const uint32_t p_tmem = tmem + (Lay::kPTmem ? Lay::col_p(t) : Lay::col_s(t)), o_tmem = tmem + Lay::col_o(t);
-        const uint64_t b0 = vst ? vd1 : vd0;
+        const uint64_t b0 = slot_desc(vd0, vd1, vst);
         if constexpr (kFp8) {  // O += P V with P (E4M3, shared memory, K-major) and V (MN-major)
           constexpr uint32_t idO8 = idesc_e4m3_f32(BM, D, 1);
           const uint64_t a0 = smem_desc_sw128(sb + Lay::kOffP + t * Lay::kPBytes, 16, 1024);
@@ -548,8 +560,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           BitWalk walk(mw, 3, n);
           for (int j = walk.next(); j >= 0; j = walk.next()) {
             const bool a0 = walk.kept(0), a1 = walk.kept(1);
-            const uint32_t kst = nk & 1, vst = kst;  // K of block j, V of the previous kept block
-            if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) {
+            const uint32_t kst = nk % Lay::kStages, vst = kst;  // K of block j, V of the previous kept block
+            if (!mbar_wait(bar(kBarKvFull + kst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) {
               ok = false;
               break;
             }
@@ -571,8 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j == last) mma_commit(bar(kBarQEmpty));
           }
           if (!ok) break;
-          const uint32_t vst = nk & 1;  // V of the last kept block alone
-          if (!mbar_wait(bar(kBarKvFull + vst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          const uint32_t vst = nk % Lay::kStages;  // V of the last kept block alone
+          if (!mbar_wait(bar(kBarKvFull + vst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (had0) {
             if (!issue_pv(0, vst, done0 > 0)) break;
@@ -612,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; ok && j <= n; ++j) {
             // step j: S_A(j), S_B(j) (j < n) and O_t += P_t(j-1) V_{j-1} (j > 0), K_j and
             // V_{j-1} in slot nk mod 2 under one barrier pair
-            const uint32_t st = nk & 1;
-            if (!mbar_wait(bar(kBarKvFull + st), (nk >> 1) & 1, abort, p.status, p.wait_ns) ||
+            const uint32_t st = nk % Lay::kStages;
+            if (!mbar_wait(bar(kBarKvFull + st), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns) ||
                 (j < nA && !early_s(0, st)) || (j < nB && !early_s(1, st))) {
               ok = false;
               break;
@@ -633,8 +645,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // j = 0
         {
-          const uint32_t kst = nk & 1;
-          if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          const uint32_t kst = nk % Lay::kStages;
+          if (!mbar_wait(bar(kBarKvFull + kst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           issue_s(0, kst);
           if (nB > 0) issue_s(1, kst);
@@ -643,8 +655,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (n == 1) mma_commit(bar(kBarQEmpty));
         }
         for (int j = 1; ok && j < n; ++j) {
-          const uint32_t kst = nk & 1, vst = kst;  // K_j and V_{j-1}: one slot, one barrier
-          if (!mbar_wait(bar(kBarKvFull + kst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) {
+          const uint32_t kst = nk % Lay::kStages, vst = kst;  // K_j and V_{j-1}: one slot, one barrier
+          if (!mbar_wait(bar(kBarKvFull + kst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -666,8 +678,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         // tail: the last P V of each tile
         {
-          const uint32_t vst = nk & 1;  // V_{n-1} alone in the item's last slot
-          if (!mbar_wait(bar(kBarKvFull + vst), (nk >> 1) & 1, abort, p.status, p.wait_ns)) break;
+          const uint32_t vst = nk % Lay::kStages;  // V_{n-1} alone in the item's last slot
+          if (!mbar_wait(bar(kBarKvFull + vst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
           if (n - 1 < nA) {
             if (!issue_pv(0, vst, n - 1 > 0)) break;
