@@ -4,12 +4,18 @@
 //   D = rowsum(dO o O),  dV += P^T dO,  dP = dO V^T,  dS = P o (dP - D),
 //   dQ += scale dS K,    dK += scale dS^T Q     (S = scale Q K^T).
 //
-// Three launches on the caller's stream:
-//   bwd_preprocess_kernel  D and -lse * log2(e) per query row, into a workspace
-//                          padded to whole 128-row tiles (pad: D = 0,
-//                          -lse log2(e) = -inf, so padded rows get P = 0);
-//                          then P = 2^(S log2(e) scale - lse log2(e)) is one
-//                          FMA and one exponential per element.
+// Two launches on the caller's stream, in this order:
+//   bwd_dq_kernel<d>       items (sequence, query head, 128-query tile i); an
+//                          item walks the key tiles j (causal: j <= i):
+//                            S = Q K_j^T, dP = dO V_j^T, dS (bf16, in two
+//                            TMEM buffers of its own), dQ += dS K_j.
+//                          Its otherwise idle warps 2-3 form D and
+//                          -lse * log2(e) of each item's rows ahead of the
+//                          element-wise warps, into a workspace padded to whole
+//                          128-row tiles (pad: D = 0, -lse log2(e) = -inf, so
+//                          padded rows get P = 0); then
+//                          P = 2^(S log2(e) scale - lse log2(e)) is one FMA and
+//                          one exponential per element.
 //   bwd_dkdv_kernel<d>     one CTA per SM over items (sequence, KV head, 128-key
 //                          tile j); an item walks the query tiles i of every
 //                          query head sharing the KV head (causal: i >= j) and
@@ -18,17 +24,14 @@
 //                            P^T (bf16, over S^T), dV += P^T dO_i,
 //                            dS^T (bf16, over dP^T), dK += dS^T Q_i;
 //                          the next S^T follows dV when its Q/dO stage has
-//                          landed (it overwrites only P^T, which dV reads).
-//   bwd_dq_kernel<d>       items (sequence, query head, 128-query tile i); an
-//                          item walks the key tiles j (causal: j <= i):
-//                            S = Q K_j^T, dP = dO V_j^T, dS (bf16, in two
-//                            TMEM buffers of its own), dQ += dS K_j.
+//                          landed (it overwrites only P^T, which dV reads); it
+//                          reads the two workspace vectors of every query tile.
 // dQ is computed in its own pass (recomputing S and dP) instead of being
 // accumulated with atomics from the dK/dV pass: at d = 128 the dK/dV pass
 // already uses all 512 TMEM columns (S^T, dP^T, dV, dK).
 //
-// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread),
-// warps 4-7 and 8-11 the element-wise work: a thread owns one TMEM lane (tile
+// Roles (384 threads): warp 0 TMA producer, warp 1 MMA issuer (one thread), in
+// the dQ pass warps 2-3 the per-row vectors, warps 4-7 and 8-11 the element-wise work: a thread owns one TMEM lane (tile
 // row), warpgroup g columns [64 g, 64 g + 64) of it. In the dK/dV pass each
 // warpgroup packs its bf16 P^T or dS^T into the first 32 columns of its own 64,
 // so the two never touch each other's columns and the MMA reads its TMEM
@@ -73,62 +76,73 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
-// ------------------------------------------------------------------ preprocess
-// A warp takes 32 consecutive query rows i0 .. i0 + 31 of one (sequence, head):
-// lane u reads the row's lse (one 128-byte read per warp), the warp walks the 32
-// rows of O and dO (each a contiguous d-long row; kRowsPerWarp rows with their
-// loads in flight together, each lane d / 32 elements of both), reduces each
-// row's dot product with shuffles and keeps row u's in lane u, and the warp
-// writes both workspace vectors with one 128-byte store each. Rows past N (the
-// padding up to Npad) get -inf and 0.
+// ------------------------------------------------------------------ per-row vectors
+// One warp forms D = rowsum(dO o O) and -lse * log2(e) for 32 consecutive query rows
+// i0 .. i0 + 31 of one (sequence, head) and writes both into the workspace: lane u
+// reads row u's lse (one 128-byte read per warp), the warp walks the 32 rows of O and
+// dO (each a contiguous d-long row; kRowsPerWarp rows with their loads in flight
+// together, each lane d / 32 elements of both), reduces each row's dot product with
+// shuffles and keeps row u's in lane u, and writes the two vectors with one 128-byte
+// store each. Rows past N (the padding up to Npad) get -inf and 0, so their P is 0.
 constexpr int kRowsPerWarp = 4;
 
 template <int D>
-__global__ void bwd_preprocess_kernel(const BwdParams p) {
+__device__ __forceinline__ void row_vectors(const BwdParams& p, int b, int h, int i0, int lane) {
   constexpr int E = D / 32;  // elements per lane: 4 (8 bytes) or 2 (4 bytes)
   using Vec = typename std::conditional<E == 4, uint2, uint32_t>::type;
-  const int lane = threadIdx.x & 31;
-  const int chunks = p.Npad / 32;                   // 32-row blocks per (sequence, head)
-  const int tasks = p.B * p.Hq * chunks;
-  const int warps = (int)((gridDim.x * blockDim.x) >> 5);
   const __nv_bfloat16* o = static_cast<const __nv_bfloat16*>(p.o);
   const __nv_bfloat16* g = static_cast<const __nv_bfloat16*>(p.dout);
-  for (int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); task < tasks; task += warps) {
-    const int bh = task / chunks, i0 = (task - bh * chunks) * 32;
-    const int b = bh / p.Hq, h = bh - b * p.Hq;
-    const int i = i0 + lane;                        // this lane's row of the block
-    const float lse = i < p.N ? __ldg(p.lse + (size_t)bh * p.N + i) : -CUDART_INF_F;
-    const int nrows = min(32, p.N - i0);            // rows of the block inside the sequence (may be <= 0)
-    float mine = 0.f;
-    for (int u0 = 0; u0 < nrows; u0 += kRowsPerWarp) {
-      Vec a[kRowsPerWarp], d[kRowsPerWarp];
+  const int bh = b * p.Hq + h;
+  const int i = i0 + lane;                        // this lane's row of the block
+  const float lse = i < p.N ? __ldg(p.lse + (size_t)bh * p.N + i) : -CUDART_INF_F;
+  const int nrows = min(32, p.N - i0);            // rows of the block inside the sequence (may be <= 0)
+  float mine = 0.f;
+  for (int u0 = 0; u0 < nrows; u0 += kRowsPerWarp) {
+    Vec a[kRowsPerWarp], d[kRowsPerWarp];
 #pragma unroll
-      for (int u = 0; u < kRowsPerWarp; ++u) {
-        if (u0 + u < nrows) {
-          const size_t off = (((size_t)b * p.N + i0 + u0 + u) * p.Hq + h) * D + lane * E;
-          a[u] = __ldg(reinterpret_cast<const Vec*>(o + off));
-          d[u] = __ldg(reinterpret_cast<const Vec*>(g + off));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kRowsPerWarp; ++u) {
-        if (u0 + u >= nrows) break;
-        const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
-        const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d[u]);
-        float dsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < E / 2; ++w) {
-          dsum = fmaf(bf16_lo(aw[w]), bf16_lo(dw[w]), dsum);
-          dsum = fmaf(bf16_hi(aw[w]), bf16_hi(dw[w]), dsum);
-        }
-#pragma unroll
-        for (int sft = 16; sft > 0; sft >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, sft);
-        if (lane == u0 + u) mine = dsum;
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      if (u0 + u < nrows) {
+        const size_t off = (((size_t)b * p.N + i0 + u0 + u) * p.Hq + h) * D + lane * E;
+        a[u] = __ldg(reinterpret_cast<const Vec*>(o + off));
+        d[u] = __ldg(reinterpret_cast<const Vec*>(g + off));
       }
     }
-    // a row with no visible key (lse = -inf), and a padding row, get P = 0
-    p.ws_nl2[(size_t)bh * p.Npad + i] = (lse > -CUDART_INF_F && lse < CUDART_INF_F) ? -lse * kLog2e : -CUDART_INF_F;
-    p.ws_d[(size_t)bh * p.Npad + i] = i < p.N ? mine : 0.f;
+#pragma unroll
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      if (u0 + u >= nrows) break;
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
+      const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d[u]);
+      float dsum = 0.f;
+#pragma unroll
+      for (int w = 0; w < E / 2; ++w) {
+        dsum = fmaf(bf16_lo(aw[w]), bf16_lo(dw[w]), dsum);
+        dsum = fmaf(bf16_hi(aw[w]), bf16_hi(dw[w]), dsum);
+      }
+#pragma unroll
+      for (int sft = 16; sft > 0; sft >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, sft);
+      if (lane == u0 + u) mine = dsum;
+    }
+  }
+  // a row with no visible key (lse = -inf), and a padding row, get P = 0
+  p.ws_nl2[(size_t)bh * p.Npad + i] = (lse > -CUDART_INF_F && lse < CUDART_INF_F) ? -lse * kLog2e : -CUDART_INF_F;
+  p.ws_d[(size_t)bh * p.Npad + i] = i < p.N ? mine : 0.f;
+}
+
+// Bounded wait until a shared-memory counter reaches `target` (abort and time limit as
+// in the mbarrier waits).
+__device__ __forceinline__ bool count_wait(volatile int* c, int target, volatile int* abort, int* status,
+                                           uint64_t limit_ns) {
+  if (*c >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(256);
+    if (*c >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_status(status, 5 /* timeout */);
+      *abort = 1;
+      return false;
+    }
   }
 }
 
@@ -575,9 +589,12 @@ struct DqLayout {
   static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
   static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
   static constexpr int kOffAbort = kOffHolder + 8;
+  // two counters: 32-row blocks whose per-row vectors are in the workspace (warps 2-3),
+  // and items the element-wise warps have started
+  static constexpr int kOffCounts = kOffAbort + 8;
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
-  static constexpr int kUsed = kOffAbort + 8 + 1024;
+  static constexpr int kUsed = kOffCounts + 8 + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory");
 };
@@ -603,11 +620,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + Lay::kOffAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  // warps 2-3: 32-row blocks whose vectors are in the workspace; element-wise warps: items started
+  volatile int* blocks_done = reinterpret_cast<volatile int*>(smem + Lay::kOffCounts);
+  volatile int* items_started = blocks_done + 1;
   if (threadIdx.x == 0) {
     for (int i = 0; i < Lay::kNumBars; ++i)
       mbar_init(bar(i), (i == kQDpFree || i == kQDsFull || i == kQAccEmpty) ? kEwArrivals : 1);
     mbar_init(bar(Lay::kBarStall), 1);
     *abort = 0;
+    *blocks_done = 0;
+    *items_started = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
@@ -748,6 +770,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_commit(bar(kQMmaDone));
       mbar_drain(bar(kQMmaDone), 0);
     }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------------------------ per-row vectors
+    // For this CTA's items in order, D and -lse log2(e) of the tile's 128 rows into the
+    // workspace (warp 2 rows 0-63, warp 3 rows 64-127), at most two items ahead of the
+    // element-wise warps; they read the vectors back once the block count shows them
+    // written, and the dK/dV pass (launched after this one) reads them all.
+    for (int kk = 0, it; (it = bwd_item_index(sch, kk)) >= 0; ++kk) {
+      if (!count_wait(items_started, kk - 1, abort, p.status, p.wait_ns)) break;
+      int b, h, i;
+      item(it, b, h, i);
+#pragma unroll 1
+      for (int blk = 0; blk < 2; ++blk) row_vectors<D>(p, b, h, i * BT + 64 * (warp - 2) + 32 * blk, lane);
+      __threadfence_block();  // the stores above before the count that announces them
+      __syncwarp();
+      if (lane == 0) atomicAdd(const_cast<int*>(blocks_done), 2);
+    }
   } else if (warp >= 4) {
     // ------------------------------------------------------------ element-wise (one query row per thread)
     const int q4 = warp & 3, wg = (warp - 4) >> 2;
@@ -769,6 +807,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jn = p.causal ? i + 1 : nt;
       const int qrow = i * BT + r;
       const size_t vrow = (size_t)(b * p.Hq + h) * p.Npad + qrow;
+      if (warp == 4 && lane == 0) atomicAdd(const_cast<int*>(items_started), 1);
+      // the item's four 32-row blocks of vectors are in the workspace
+      if (!count_wait(blocks_done, 4 * (kk + 1), abort, p.status, p.wait_ns)) break;
+      __threadfence_block();
       const float nl2 = p.ws_nl2[vrow], dval = p.ws_d[vrow];
       const uint64_t nl2x2 = f2_pack(nl2, nl2);
       for (int j = 0; j < jn; ++j) {
@@ -844,13 +886,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                          const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
-  const long long tasks = (long long)p.B * p.Hq * (p.Npad / 32);  // 32-row blocks, 8 per 256-thread block
-  const int pre_blocks = (int)std::min<long long>((tasks + 7) / 8, (long long)num_sms * 16);
-  bwd_preprocess_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
   const int nt = (p.N + BT - 1) / BT;
+  cudaError_t e;
+  {  // dQ, and the two per-row vectors the dK/dV pass reads
+    auto kern = bwd_dq_kernel<D>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::kBytes);
+    if (e != cudaSuccess) return e;
+    const long long items = (long long)p.B * p.Hq * nt;
+    const int grid = (int)std::min<long long>(items, num_sms);
+    kern<<<grid, kThreads, DqLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   {
     auto kern = bwd_dkdv_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DkdvLayout<D>::kBytes);
@@ -858,16 +905,6 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtens
     const long long items = (long long)p.B * p.Hkv * nt;
     const int grid = (int)std::min<long long>(items, num_sms);
     kern<<<grid, kThreads, DkdvLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
-  {
-    auto kern = bwd_dq_kernel<D>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqLayout<D>::kBytes);
-    if (e != cudaSuccess) return e;
-    const long long items = (long long)p.B * p.Hq * nt;
-    const int grid = (int)std::min<long long>(items, num_sms);
-    kern<<<grid, kThreads, DqLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
     e = cudaGetLastError();
   }
   return e;

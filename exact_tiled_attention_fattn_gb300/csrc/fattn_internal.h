@@ -123,7 +123,8 @@ struct BwdParams {
   int debug_stall;
 };
 
-// Preprocess, dK/dV pass and dQ pass, in that order on `stream`. Tensor maps
+// dQ pass (which also writes the workspace's two vectors) and dK/dV pass, in that
+// order on `stream`. Tensor maps
 // are over the packed [B * N, H, d] views of q, k, v and dout (128-row boxes).
 cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, int num_sms, cudaStream_t stream);
