@@ -84,7 +84,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
 // together, each lane d / 32 elements of both), reduces each row's dot product with
 // shuffles and keeps row u's in lane u, and writes the two vectors with one 128-byte
 // store each. Rows past N (the padding up to Npad) get -inf and 0, so their P is 0.
-constexpr int kRowsPerWarp = 4;
+constexpr int kRowsPerWarp = 8;
 
 template <int D>
 __device__ __forceinline__ void row_vectors(const BwdParams& p, int b, int h, int i0, int lane) {
