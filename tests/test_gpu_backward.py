@@ -28,6 +28,9 @@ CASES = [
     (2, 256, 2, 2, 128, False),
     (1, 100, 1, 1, 64, False),
     (1, 1000, 4, 4, 128, True),
+    # shorter than one tile: most of the per-row vectors are padding (-inf, 0)
+    (2, 17, 2, 1, 128, True),
+    (1, 1, 2, 2, 64, False),
 ]
 
 

@@ -73,7 +73,9 @@ def _flat(o, lse, rows):
     return og[rows[:, 0], rows[:, 2], rows[:, 1]], lg[rows[:, 0], rows[:, 1], rows[:, 2]]
 
 
-CASES = [(2, 300, 4, 2, True), (1, 513, 8, 1, True), (2, 256, 2, 2, False), (1, 1000, 4, 4, True)]
+CASES = [(2, 300, 4, 2, True), (1, 513, 8, 1, True), (2, 256, 2, 2, False), (1, 1000, 4, 4, True),
+         # shorter than one tile: V rows past N come from the next sequence (times P = 0) or as zeros
+         (3, 37, 2, 1, True), (2, 1, 2, 2, False)]
 
 
 @pytest.mark.parametrize("B,N,Hq,Hkv,causal", CASES)

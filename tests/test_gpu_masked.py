@@ -35,6 +35,8 @@ CASES = [
     (1, 513, 8, 1, 64, True, 1, 8),
     (2, 256, 2, 2, 64, False, 2, 1),
     (1, 1000, 2, 2, 128, True, 1, 1),
+    # shorter than one tile; rows 32 entries long (32-byte loads of 16-key groups)
+    (2, 24, 2, 2, 128, True, 2, 1),
 ]
 
 
