@@ -4,9 +4,11 @@
 //
 // One CTA per SM loops over work items (sequence, query head, 256 query rows =
 // two 128-row Q tiles A and B that share every K/V tile). Roles:
-//   warp 0      TMA producer: Q_A and Q_B once per item, then K_j / V_j tiles
-//               into two 2-stage rings (128-byte swizzle, 64-column boxes); the
-//               K_j and V_{j-1} of one step share one slot's full / empty barriers.
+//   warp 0      TMA producer: Q_A and Q_B once per item, then per step j the
+//               tiles K_j and V_{j-1} into one slot of a ring (two slots; three
+//               in the FP8 variant, whose tiles are half the size) under that
+//               slot's full / empty barrier pair (128-byte swizzle, 64-column
+//               boxes).
 //   warp 1      MMA issuer (one thread). Per K/V tile j it issues
 //               O_A += P_A(j-1) V_{j-1}, S_A = Q_A K_j^T, O_B += P_B(j-1) V_{j-1},
 //               S_B = Q_B K_j^T, so that while one softmax warpgroup works on its
@@ -35,6 +37,14 @@
 // of the two tiles' kept blocks in the same interleaved order, each softmax
 // warpgroup walks its own row, and a tile whose rows keep no block writes
 // O = 0, lse = -inf.
+// Paged variant ("Paged variants"): K/V tiles come page by page through the
+// block table, eight producer lanes each issuing one page's box. Masked variant
+// (the formula's additive M): each softmax thread adds its row's bf16 mask
+// entries to the scaled scores, the first 64 keys of a tile by 32- or 16-byte
+// loads into registers, the other 64 copied by the warp into its staging slot,
+// both requested before the wait for the scores. FP8 variant (FlashAttention-3
+// row of "The FlashAttention family"): E4M3 Q, K and V (kind::f8f6f4 products,
+// V read in place as an MN-major operand), P rounded to E4M3 in shared memory.
 //
 // P_X aliases S_X: S_X(j) is issued right after O_X += P_X(j-1) V by the same
 // thread, and tcgen05.mma operations issued by one thread execute in order, so
