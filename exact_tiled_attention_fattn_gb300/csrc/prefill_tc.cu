@@ -309,6 +309,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kPaged = kMode == kModePaged;    // K/V through a block table
   constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
   constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V; P in E4M3 through shared memory
+  // key tiles visited from the last (the diagonal under the causal rule) down to 0, so that the
+  // two tiles of an item finish together (block-sparse: in mask order)
+  constexpr bool kReverse = !kSparse;
   static_assert(!kFp8 || D == 128, "FP8 tiles are 128 one-byte columns: one 128-byte swizzle span");
   constexpr int kChunks = kFp8 ? 1 : D / 64;      // 128-byte boxes per tile row
   using Lay = TcLayout<D, kMode>;
@@ -458,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             if (leader) mbar_arrive_expect_tx(bar(kBarKvFull + st), ((s < n) + (s > 0)) * Lay::kKVBytes);
-            if (s < n) issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKvFull + st), s, false);
-            if (s > 0) issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarKvFull + st), s - 1, true);
+            if (s < n) issue_kv(&tk, sb + Lay::kOffK + st * Lay::kKVBytes, bar(kBarKvFull + st), kReverse ? n - 1 - s : s, false);
+            if (s > 0) issue_kv(&tv, sb + Lay::kOffV + st * Lay::kKVBytes, bar(kBarKvFull + st), kReverse ? n - s : s - 1, true);
             ++nk;
           }
         }
@@ -612,6 +615,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int nA = x.n[0], nB = x.n[1];
         const int n = max(nA, nB);
+        // tile t takes part in steps [f_t, f_t + n_t) (reverse order: the last n_t steps)
+        const int fA = kReverse ? n - nA : 0, fB = kReverse ? n - nB : 0;
+        auto in_a = [&](int s) { return s >= fA && s < fA + nA; };
+        auto in_b = [&](int s) { return s >= fB && s < fB + nB; };
         if (!mbar_wait(bar(kBarQFull), nq & 1, abort, p.status, p.wait_ns)) break;
         ++nq;
         tc_fence_after();
@@ -636,14 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // V_{j-1} in slot nk mod 2 under one barrier pair
             const uint32_t st = nk % Lay::kStages;
             if (!mbar_wait(bar(kBarKvFull + st), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns) ||
-                (j < nA && !early_s(0, st)) || (j < nB && !early_s(1, st))) {
+                (in_a(j) && !early_s(0, st)) || (in_b(j) && !early_s(1, st))) {
               ok = false;
               break;
             }
             if (j == n - 1) mma_commit(bar(kBarQEmpty));
             if (j > 0) {
               tc_fence_after();
-              if ((j - 1 < nA && !early_pv(0, st, j - 1 > 0)) || (j - 1 < nB && !early_pv(1, st, j - 1 > 0))) {
+              if ((in_a(j - 1) && !early_pv(0, st, j - 1 > fA)) || (in_b(j - 1) && !early_pv(1, st, j - 1 > fB))) {
                 ok = false;
                 break;
               }
@@ -658,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kst = nk % Lay::kStages;
           if (!mbar_wait(bar(kBarKvFull + kst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
-          issue_s(0, kst);
-          if (nB > 0) issue_s(1, kst);
+          if (in_a(0)) issue_s(0, kst);
+          if (in_b(0)) issue_s(1, kst);
           mma_commit(bar(kBarKvEmpty + kst));
           ++nk;
           if (n == 1) mma_commit(bar(kBarQEmpty));
@@ -671,16 +678,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          if (j - 1 < nA) {
-            if (!issue_pv(0, vst, j - 1 > 0)) { ok = false; break; }
-            if (j - 1 == nA - 1) mma_commit(bar(kBarOFull + 0));
+          if (in_a(j - 1)) {
+            if (!issue_pv(0, vst, j - 1 > fA)) { ok = false; break; }
+            if (j - 1 == fA + nA - 1) mma_commit(bar(kBarOFull + 0));
           }
-          if (j < nA) issue_s(0, kst);
-          if (j - 1 < nB) {
-            if (!issue_pv(1, vst, j - 1 > 0)) { ok = false; break; }
-            if (j - 1 == nB - 1) mma_commit(bar(kBarOFull + 1));
+          if (in_a(j)) issue_s(0, kst);
+          if (in_b(j - 1)) {
+            if (!issue_pv(1, vst, j - 1 > fB)) { ok = false; break; }
+            if (j - 1 == fB + nB - 1) mma_commit(bar(kBarOFull + 1));
           }
-          if (j < nB) issue_s(1, kst);
+          if (in_b(j)) issue_s(1, kst);
           mma_commit(bar(kBarKvEmpty + kst));
           ++nk;
           if (j == n - 1) mma_commit(bar(kBarQEmpty));
@@ -691,12 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t vst = nk % Lay::kStages;  // V_{n-1} alone in the item's last slot
           if (!mbar_wait(bar(kBarKvFull + vst), (nk / Lay::kStages) & 1, abort, p.status, p.wait_ns)) break;
           tc_fence_after();
-          if (n - 1 < nA) {
-            if (!issue_pv(0, vst, n - 1 > 0)) break;
+          if (in_a(n - 1)) {
+            if (!issue_pv(0, vst, n - 1 > fA)) break;
             mma_commit(bar(kBarOFull + 0));
           }
-          if (n - 1 < nB) {
-            if (!issue_pv(1, vst, n - 1 > 0)) break;
+          if (in_b(n - 1)) {
+            if (!issue_pv(1, vst, n - 1 > fB)) break;
             mma_commit(bar(kBarOFull + 1));
           }
           mma_commit(bar(kBarKvEmpty + vst));
@@ -830,7 +837,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mrow = static_cast<const __nv_bfloat16*>(p.mask) + (size_t)x.b * p.mask_sb + (size_t)x.h * p.mask_sh +
                (size_t)min(row, x.L - 1) * p.mask_ld;
       BitWalk walk(mw, 1 << t, nt);
-      for (int j = kSparse ? walk.next() : 0; kSparse ? j >= 0 : j < nt; j = kSparse ? walk.next() : j + 1) {
+      for (int j = kSparse ? walk.next() : (kReverse ? nt - 1 : 0); kSparse || kReverse ? j >= 0 : j < nt;
+           j = kSparse ? walk.next() : (kReverse ? j - 1 : j + 1)) {
         // the tile's 128 mask entries, requested before waiting for S (16-byte loads
         // of whole 8-key groups; groups at or past the visible limit are not read)
         uint4 mv[kMasked ? BN / 16 : 1];
