@@ -32,7 +32,7 @@
 // the diagonal are never touched"). S and P never leave the SM.
 // Block-sparse variant ("Block-sparse FlashAttention": zero blocks of a fixed
 // block mask are skipped): with 128 x 128 blocks, a tile visits only the K/V
-// blocks its mask row keeps; warp 2 turns the item's two mask rows into bit
+// blocks its mask row keeps (highest first); warp 2 turns the item's two mask rows into bit
 // words in a shared-memory ring, the producer and the MMA warp walk the union
 // of the two tiles' kept blocks in the same interleaved order, each softmax
 // warpgroup walks its own row, and a tile whose rows keep no block writes
@@ -98,7 +98,7 @@ constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exc
 // Block-mask ring (block-sparse variant): warp 2 reads the two mask rows of
 // each item into bit words (bit j of row t: tile t keeps K/V block j, already
 // clipped to the blocks the tile visits), with the kept-block counts and the
-// last block either tile keeps. Producer, MMA issuer and softmax warps walk
+// highest and lowest blocks either tile keeps. Producer, MMA issuer and softmax warps walk
 // the bits from shared memory, so no mask load sits on their paths.
 constexpr int kMaskSlots = 4;
 constexpr int kMaskWords = 64;                        // up to 2048 blocks per row
@@ -257,24 +257,25 @@ __device__ __forceinline__ Item decode_item(const PrefillParams& p, const Schedu
 }
 
 // Walks the kept blocks of one mask row (sel = 1 << t) or of the union of both
-// rows (sel = 3) in increasing order. The current word of each row is held in
-// registers, so a step costs a find-first-set; shared memory is read once per
-// 32 blocks. Bits past a row's n[t] are zero, so the walk ends by itself.
+// rows (sel = 3) in decreasing order (the diagonal block first under the causal
+// rule, as the dense variants visit their key tiles). The current word of each row
+// is held in registers, so a step costs a count-leading-zeros; shared memory is
+// read once per 32 blocks. Bits past a row's n[t] are zero.
 struct BitWalk {
   const uint32_t* w;
-  int sel, nw, wi, bit;
+  int sel, wi, bit;
   uint32_t u0, u1, rem;
   __device__ __forceinline__ BitWalk(const uint32_t* words, int sel_, int end)
-      : w(words), sel(sel_), nw((end + 31) >> 5), wi(-1), bit(0), u0(0), u1(0), rem(0) {}
+      : w(words), sel(sel_), wi((end + 31) >> 5), bit(0), u0(0), u1(0), rem(0) {}
   __device__ __forceinline__ int next() {  // next kept block, or -1
     while (rem == 0) {
-      if (++wi >= nw) return -1;
+      if (--wi < 0) return -1;
       u0 = (sel & 1) ? w[wi] : 0u;
       u1 = (sel & 2) ? w[kMaskWords + wi] : 0u;
       rem = u0 | u1;
     }
-    bit = __ffs(rem) - 1;
-    rem &= rem - 1;
+    bit = 31 - __clz(rem);
+    rem &= ~(1u << bit);
     return wi * 32 + bit;
   }
   __device__ __forceinline__ bool kept(int t) const { return ((t ? u1 : u0) >> bit) & 1u; }
@@ -310,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool kMasked = kMode == kModeMasked;  // additive bf16 mask M on the scores
   constexpr bool kFp8 = kMode == kModeFp8;        // E4M3 Q, K, V; P in E4M3 through shared memory
   // key tiles visited from the last (the diagonal under the causal rule) down to 0, so that the
-  // two tiles of an item finish together (block-sparse: in mask order)
+  // two tiles of an item finish together (block-sparse: the bit walks go down likewise)
   constexpr bool kReverse = !kSparse;
   static_assert(!kFp8 || D == 128, "FP8 tiles are 128 one-byte columns: one 128-byte swizzle span");
   constexpr int kChunks = kFp8 ? 1 : D / 64;      // 128-byte boxes per tile row
@@ -558,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           const uint32_t* mw = mask_slot(nm);
           const int cnt[2] = {(int)mw[2 * kMaskWords], (int)mw[2 * kMaskWords + 1]};
-          const int last = (int)mw[2 * kMaskWords + 2];
+          const int last = (int)mw[2 * kMaskWords + 2], low = (int)mw[2 * kMaskWords + 3];
           if (last < 0) {  // the producer loads no Q for this item
             mbar_arrive(bar(kBarMaskEmpty + nm % kMaskSlots));
             ++nm;
@@ -593,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             had1 = a1;
             mma_commit(bar(kBarKvEmpty + kst));
             ++nk;
-            if (j == last) mma_commit(bar(kBarQEmpty));
+            if (j == low) mma_commit(bar(kBarQEmpty));  // the walk's last block
           }
           if (!ok) break;
           const uint32_t vst = nk % Lay::kStages;  // V of the last kept block alone
@@ -728,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!warp_wait(bar(kBarMaskEmpty + nm % kMaskSlots), ((nm / kMaskSlots) & 1) ^ 1, abort, p.status, p.wait_ns)) break;
       uint32_t* w = reinterpret_cast<uint32_t*>(smem + Lay::kOffMask + (nm % kMaskSlots) * kMaskSlotBytes);
       const int nw = (max(x.n[0], x.n[1]) + 31) >> 5;   // <= kMaskWords: nb <= kSparseMaxBlocks
-      int cnt[2] = {0, 0}, last = -1;
+      int cnt[2] = {0, 0}, last = -1, low = 1 << 30;
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         const uint8_t* mrow = p.block_mask + ((size_t)(x.h % p.mask_heads) * nb + (x.base / BM + t)) * nb;
@@ -745,7 +746,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (w0 + i < nw) {
               if (lane == 0) w[t * kMaskWords + w0 + i] = bits;
               cnt[t] += __popc(bits);
-              if (bits) last = max(last, (w0 + i) * 32 + 31 - __clz(bits));
+              if (bits) {
+                last = max(last, (w0 + i) * 32 + 31 - __clz(bits));
+                low = min(low, (w0 + i) * 32 + __ffs(bits) - 1);
+              }
             }
           }
         }
@@ -754,6 +758,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         w[2 * kMaskWords] = (uint32_t)cnt[0];
         w[2 * kMaskWords + 1] = (uint32_t)cnt[1];
         w[2 * kMaskWords + 2] = (uint32_t)last;
+        w[2 * kMaskWords + 3] = (uint32_t)low;   // the walk's last block (it goes down)
         mbar_arrive(bar(kBarMaskFull + nm % kMaskSlots));  // release: the words above are visible
       }
       __syncwarp();
