@@ -686,8 +686,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(bar(kQKvFull + vs), 2 * Lay::kTile);
-          load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kQKvFull + vs), hkv, b * p.N + j * BT, pol_kv);
-          load_tile<D>(sb + Lay::kOffV + vs * Lay::kTile, &tv, bar(kQKvFull + vs), hkv, b * p.N + j * BT, pol_kv);
+          const int kt = jn - 1 - j;  // key tiles from the diagonal down
+          load_tile<D>(sb + Lay::kOffK + ks * Lay::kTile, &tk, bar(kQKvFull + vs), hkv, b * p.N + kt * BT, pol_kv);
+          load_tile<D>(sb + Lay::kOffV + vs * Lay::kTile, &tv, bar(kQKvFull + vs), hkv, b * p.N + kt * BT, pol_kv);
           ++nk;
           ++nv;
         }
@@ -825,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t u[64];
           tmem_ld64(s_col, u);
           // visible keys of this tile: column c < lim
-          const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - j * BT - cb;
+          const int lim = min(p.causal ? qrow + 1 : p.N, p.N) - (jn - 1 - j) * BT - cb;  // key tile jn - 1 - j
 #pragma unroll
           for (int c = 0; c < 64; c += 2) {
             float x0, x1;
