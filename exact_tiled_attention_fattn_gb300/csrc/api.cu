@@ -354,13 +354,14 @@ extern "C" fattn_status fattn_bwd(const void* q, const void* k, const void* v, c
   p.status = status_ptr(&err);
   if (err) return FATTN_ERR_CUDA;
   set_waits(p);
-  CUtensorMap tq, tk, tv, tdo;
+  CUtensorMap tq, tk, tv, tdo, tdk, tdv;
   if (!encode_rows_map(&tq, q, (int)rows, Hq, d, 128) || !encode_rows_map(&tk, k, (int)rows, Hkv, d, 128) ||
-      !encode_rows_map(&tv, v, (int)rows, Hkv, d, 128) || !encode_rows_map(&tdo, dout, (int)rows, Hq, d, 128))
+      !encode_rows_map(&tv, v, (int)rows, Hkv, d, 128) || !encode_rows_map(&tdo, dout, (int)rows, Hq, d, 128) ||
+      !encode_rows_map(&tdk, dk, (int)rows, Hkv, d, 32) || !encode_rows_map(&tdv, dv, (int)rows, Hkv, d, 32))
     return FATTN_ERR_CUDA;
   const int sms = num_sms_current();
   if (sms <= 0) return FATTN_ERR_CUDA;
-  return launch_backward(p, tq, tk, tv, tdo, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
+  return launch_backward(p, tq, tk, tv, tdo, tdk, tdv, sms, stream) == cudaSuccess ? FATTN_OK : FATTN_ERR_CUDA;
 }
 
 extern "C" size_t fattn_decode_workspace_size(int B, int Hq, int d, int num_splits) {

@@ -15,7 +15,9 @@
 //                          128-row tiles (pad: D = 0, -lse log2(e) = -inf, so
 //                          padded rows get P = 0); then
 //                          P = 2^(S log2(e) scale - lse log2(e)) is one FMA and
-//                          one exponential per element.
+//                          one exponential per element. An item's dQ is written
+//                          after the next item's first key tile, while that
+//                          item's next S and dP run.
 //   bwd_dkdv_kernel<d>     one CTA per SM over items (sequence, KV head, 128-key
 //                          tile j); an item walks the query tiles i of every
 //                          query head sharing the KV head (causal: i >= j) and
@@ -26,6 +28,12 @@
 //                          the next S^T follows dV when its Q/dO stage has
 //                          landed (it overwrites only P^T, which dV reads); it
 //                          reads the two workspace vectors of every query tile.
+//                          dV is written while the item's last dK product
+//                          runs, then dK (d = 128: staged in shared memory and
+//                          stored by TMA, 32 rows x 64 columns per warp).
+// In both passes an item's resident tiles (K_j, V_j; Q_i, dO_i) are released as
+// soon as the last product that reads them completes, so the next item's load
+// overlaps the item's last products.
 // dQ is computed in its own pass (recomputing S and dP) instead of being
 // accumulated with atomics from the dK/dV pass: at d = 128 the dK/dV pass
 // already uses all 512 TMEM columns (S^T, dP^T, dV, dK).
@@ -301,33 +309,46 @@ struct DkdvLayout {
   static constexpr int kOffRing = 2 * kTile;      // stage s: Q_i, dO_i, -lse log2(e) [128], D[128]
   static constexpr int kStage = 2 * kTile + 1024;
   static constexpr int kStages = 2;
-  static constexpr int kOffBar = kOffRing + kStages * kStage;
-  static constexpr int kNumBars = 13;
+  // d = 128: each element-wise warp stages 32 rows x 64 columns of dV, then of dK (bf16,
+  // 128-byte swizzle) in a 4 KB slot of its own and stores them with one TMA box each
+  static constexpr bool kStoreTma = D == 128;
+  static constexpr int kOutSlot = 32 * 128;
+  static constexpr int kOffOut = kOffRing + kStages * kStage;
+  static constexpr int kEnd = kOffOut + (kStoreTma ? 8 * kOutSlot : 0);
+  // barriers, the TMEM address and the abort flag (8-byte words) sit in whichever end of
+  // the 1 KB alignment slack has room for them: before the aligned base if the slack
+  // there is at least kSmallBytes, else after kEnd (where 1 KB minus that slack remains)
+  static constexpr int kNumBars = 14;
   static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
-  static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
+  static constexpr int kOffHolder = (kNumBars + 1) * 8;  // from the start of the small words
   static constexpr int kOffAbort = kOffHolder + 8;
+  static constexpr int kSmallBytes = kOffAbort + 8;
+  static_assert(2 * kSmallBytes <= 1024, "small words in the slack");
   // + slack to align the base to 1024 B; at least 117 KB so that a second CTA
   // (which would wait in tcgen05.alloc for all 512 columns) never shares the SM
-  static constexpr int kUsed = kOffAbort + 8 + 1024;
+  static constexpr int kUsed = kEnd + 1024;
   static constexpr int kBytes = kUsed > 117 * 1024 ? kUsed : 117 * 1024;
   static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 enum : int {
   kKvFull = 0, kKvEmpty = 1, kQdFull = 2, kQdEmpty = 4, kSFull = 6, kDpFull = 7, kPFull = 8, kDsFull = 9,
-  kAccFull = 10, kAccEmpty = 11, kMmaDone = 12
+  kAccFull = 10, kAccEmpty = 11, kMmaDone = 12, kDvFull = 13
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const __grid_constant__ CUtensorMap tdk, const __grid_constant__ CUtensorMap tdv,
                     const BwdParams p) {
   using Lay = DkdvLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
-  auto bar = [&](int i) -> uint32_t { return sb + Lay::kOffBar + 8 * i; };
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + Lay::kOffAbort);
+  uint8_t* small = smem - smem_raw >= Lay::kSmallBytes ? smem_raw : smem + Lay::kEnd;
+  const uint32_t ssb = smem_u32(small);
+  auto bar = [&](int i) -> uint32_t { return ssb + 8 * i; };
+  volatile int* abort = reinterpret_cast<volatile int*>(small + Lay::kOffAbort);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -342,15 +363,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
+    if constexpr (Lay::kStoreTma) {
+      tma_prefetch_desc(&tdk);
+      tma_prefetch_desc(&tdv);
+    }
   }
   if (warp == 1) {
-    tmem_alloc(sb + Lay::kOffHolder, kTmemCols);
+    tmem_alloc(ssb + Lay::kOffHolder, kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(smem + Lay::kOffHolder);
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(small + Lay::kOffHolder);
 
   const int nt = (p.N + BT - 1) / BT;
   const int G = p.Hq / p.Hkv;
@@ -432,6 +457,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           issue_kk<D>(tDP, vd, dok);  // dP^T = V dO^T (dS^T of the previous step was read by its dK product)
           mma_commit(bar(kDpFull));
+          // the item's last product that reads K_j or V_j: the next item's tiles may load
+          // as soon as it completes, while this item's last dV and dK run
+          if (t + 1 == steps) mma_commit(bar(kKvEmpty));
           if (t == 0 && !mbar_wait(bar(kAccEmpty), (nacc & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
             break;
@@ -443,6 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++np;
           tc_fence_after();
           issue_tn<D>(tDV, tS, domn, t > 0);  // dV += P^T dO
+          if (t + 1 == steps) mma_commit(bar(kDvFull));  // the item's dV is complete
           // The next S^T may follow right away if its Q stage has landed: it overwrites
           // P^T, which only the dV product just issued reads (the element-wise warps keep
           // P^T in registers for dS^T), and runs while they compute dS^T. Otherwise it
@@ -468,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nqd;
         }
         if (!ok) break;
-        mma_commit(bar(kKvEmpty));
+        if (steps == 0) mma_commit(bar(kKvEmpty));
         mma_commit(bar(kAccFull));
         ++nacc;
       }
@@ -482,7 +511,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cb = 64 * wg;                          // this warpgroup's query columns
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
     const uint32_t s_col = tmem + lane_off + kColS + cb, dp_col = tmem + lane_off + kColDP + cb;
-    const uint32_t acc_col = tmem + lane_off + kColAcc + (wg ? D : 0);  // warpgroup 0 writes dV, 1 writes dK
+    const uint32_t acc_col = tmem + lane_off + kColAcc;  // dV, then dK at + D
+    // this warp's output slot (d = 128): row `lane` at 128 lane, 16-byte chunk c at
+    // c ^ (lane mod 8), the 128-byte swizzle of the dK and dV tensor maps
+    uint8_t* slot = smem + Lay::kOffOut + (warp - 4) * Lay::kOutSlot;
+    const uint32_t slot_s = sb + Lay::kOffOut + (warp - 4) * Lay::kOutSlot;
+    // 64 accumulator columns of this thread's row, times mul, in bf16 into the slot, then
+    // one TMA store of the warp's 32 x 64 box at (column c0, head h, row row0)
+    auto stage_out = [&](uint32_t t_col, float mul, const CUtensorMap* map, int c0, int h, int row0) {
+      if (lane == 0) bulk_wait_read_all();  // the slot's previous store has read it
+      __syncwarp();
+#pragma unroll
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t u[32];
+        tmem_ld32(t_col + 32 * c2, u);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          uint32_t w[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = pack_bf16x2(__uint_as_float(u[8 * e + 2 * i]) * mul, __uint_as_float(u[8 * e + 2 * i + 1]) * mul);
+          const int chunk = 4 * c2 + e;
+          *reinterpret_cast<uint4*>(slot + lane * 128 + ((chunk ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_3d(map, slot_s, c0, h, row0);
+        bulk_commit_group();
+      }
+    };
     const float sl2 = p.scale * kLog2e;
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t nqd = 0, ns = 0, ndp = 0, nacc = 0;
@@ -551,18 +610,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nqd;
       }
       if (!ok) break;
-      // epilogue: warpgroup 0 writes dV, warpgroup 1 scale * dK, one key row per thread
-      if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status, p.wait_ns)) break;
-      ++nacc;
+      // epilogue, one key row per thread, warpgroup g columns [g D / 2, (g + 1) D / 2) of it:
+      // dV as soon as the item's last dV product has completed (while its last dK product
+      // runs), then scale * dK; at d = 128 through the warp's slot and a TMA store when
+      // all 32 of the warp's key rows lie in the sequence
+      if (!warp_wait(bar(kDvFull), nacc & 1, abort, p.status, p.wait_ns)) break;
       tc_fence_after();
       const int key = j * BT + r;
       const bool live = key < p.N;
-      const size_t off = (((size_t)b * p.N + (live ? key : 0)) * p.Hkv + hkv) * D;
-      store_row<D>(acc_col, wg ? p.scale : 1.f, static_cast<__nv_bfloat16*>(wg ? p.dk : p.dv) + off, live);
+      const size_t off = (((size_t)b * p.N + (live ? key : 0)) * p.Hkv + hkv) * D + wg * (D / 2);
+      const int wkey0 = j * BT + q4 * 32;  // the warp's first key row
+      const bool staged = Lay::kStoreTma && wkey0 + 32 <= p.N;
+      if (staged)
+        stage_out(acc_col + wg * (D / 2), 1.f, &tdv, wg * (D / 2), hkv, b * p.N + wkey0);
+      else
+        store_row<D / 2>(acc_col + wg * (D / 2), 1.f, static_cast<__nv_bfloat16*>(p.dv) + off, live);
+      if (!warp_wait(bar(kAccFull), nacc & 1, abort, p.status, p.wait_ns)) break;
+      ++nacc;
+      tc_fence_after();
+      if (staged)
+        stage_out(acc_col + D + wg * (D / 2), p.scale, &tdk, wg * (D / 2), hkv, b * p.N + wkey0);
+      else
+        store_row<D / 2>(acc_col + D + wg * (D / 2), p.scale, static_cast<__nv_bfloat16*>(p.dk) + off, live);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(kAccEmpty));
     }
+    // the TMA stores complete before the CTA (and its slots) goes away
+    if (Lay::kStoreTma && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -739,6 +814,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(kQFull), nq & 1, abort, p.status, p.wait_ns)) break;
         ++nq;
         if (!issue_s(n) || !issue_dp(n)) break;
+        // Q and dO are read by the item's S and dP products alone: once the last of them
+        // completes, the next item's tiles may load while this item's last dQ runs
+        if (jn == 1) mma_commit(bar(kQEmpty));
         for (int j = 0; j < jn; ++j, ++n) {
           if (j + 1 < jn) {  // S_n and dP_n both read: the next two products may overwrite them
             if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns) || !issue_s(n + 1) ||
@@ -747,6 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             ++ndpf;
+            if (j + 2 == jn) mma_commit(bar(kQEmpty));
           }
           if (j == 0 && !mbar_wait(bar(kQAccEmpty), (nacc & 1) ^ 1, abort, p.status, p.wait_ns)) {
             ok = false;
@@ -764,7 +843,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the item's last S and dP were read before its last dS was written
         if (!mbar_wait(bar(kQDpFree), ndpf & 1, abort, p.status, p.wait_ns)) break;
         ++ndpf;
-        mma_commit(bar(kQEmpty));
         mma_commit(bar(kQAccFull));
         ++nacc;
       }
@@ -799,6 +877,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t sl2x2 = f2_pack(sl2, sl2);
     uint32_t ns = 0, ndp = 0, nacc = 0;
     bool ok = true;
+    // The epilogue of an item (dQ in bf16, warpgroup g columns [g D / 2, (g + 1) D / 2) of
+    // the row) runs after the first key tile of the next item, so that it overlaps that
+    // item's next S and dP products instead of holding up its first ones.
+    int pend = -1, pb = 0, ph = 0;  // query tile of the item whose epilogue is pending (-1: none)
+    auto epilogue = [&]() -> bool {
+      if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status, p.wait_ns)) return false;
+      ++nacc;
+      tc_fence_after();
+      const int prow = pend * BT + r;
+      const bool live = prow < p.N;
+      const size_t off = (((size_t)pb * p.N + (live ? prow : 0)) * p.Hq + ph) * D + wg * (D / 2);
+      store_row<D / 2>(dq_col + wg * (D / 2), p.scale, static_cast<__nv_bfloat16*>(p.dq) + off, live);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kQAccEmpty));
+      pend = -1;
+      return true;
+    };
     // test hook: a wait that runs out (nothing arrives on the stall barrier), after which
     // every role stops, drains and frees TMEM; the outputs stay unwritten
     if (p.debug_stall && !warp_wait(bar(Lay::kBarStall), 0, abort, p.status, p.wait_ns)) ok = false;
@@ -861,19 +957,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(kQDsFull));
+        // the previous item's dQ: its accumulator is free for this item's first dQ product
+        if (j == 0 && pend >= 0 && !epilogue()) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
-      if (!warp_wait(bar(kQAccFull), nacc & 1, abort, p.status, p.wait_ns)) break;
-      ++nacc;
-      tc_fence_after();
-      // warpgroup g writes columns [g D / 2, (g + 1) D / 2) of its row
-      const bool live = qrow < p.N;
-      const size_t off = (((size_t)b * p.N + (live ? qrow : 0)) * p.Hq + h) * D + wg * (D / 2);
-      store_row<D / 2>(dq_col + wg * (D / 2), p.scale, static_cast<__nv_bfloat16*>(p.dq) + off, live);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kQAccEmpty));
+      pend = i;
+      pb = b;
+      ph = h;
     }
+    if (ok && pend >= 0) epilogue();
   }
 
   tc_fence_before();
@@ -886,7 +981,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
+                         const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, int num_sms,
+                         cudaStream_t stream) {
   const int nt = (p.N + BT - 1) / BT;
   cudaError_t e;
   {  // dQ, and the two per-row vectors the dK/dV pass reads
@@ -905,7 +1001,7 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtens
     if (e != cudaSuccess) return e;
     const long long items = (long long)p.B * p.Hkv * nt;
     const int grid = (int)std::min<long long>(items, num_sms);
-    kern<<<grid, kThreads, DkdvLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, p);
+    kern<<<grid, kThreads, DkdvLayout<D>::kBytes, stream>>>(tq, tk, tv, tdo, tdk, tdv, p);
     e = cudaGetLastError();
   }
   return e;
@@ -914,9 +1010,10 @@ cudaError_t launch_bwd_t(const BwdParams& p, const CUtensorMap& tq, const CUtens
 }  // namespace
 
 cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, int num_sms, cudaStream_t stream) {
-  if (p.d == 128) return launch_bwd_t<128>(p, tq, tk, tv, tdo, num_sms, stream);
-  return launch_bwd_t<64>(p, tq, tk, tv, tdo, num_sms, stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, int num_sms,
+                            cudaStream_t stream) {
+  if (p.d == 128) return launch_bwd_t<128>(p, tq, tk, tv, tdo, tdk, tdv, num_sms, stream);
+  return launch_bwd_t<64>(p, tq, tk, tv, tdo, tdk, tdv, num_sms, stream);
 }
 
 }  // namespace fattn

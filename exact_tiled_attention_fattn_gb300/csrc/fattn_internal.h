@@ -124,9 +124,10 @@ struct BwdParams {
 };
 
 // dQ pass (which also writes the workspace's two vectors) and dK/dV pass, in that
-// order on `stream`. Tensor maps
-// are over the packed [B * N, H, d] views of q, k, v and dout (128-row boxes).
+// order on `stream`. Tensor maps are over the packed [B * N, H, d] views of q, k, v
+// and dout (128-row boxes) and of dk and dv (32-row boxes, for the stores).
 cudaError_t launch_backward(const BwdParams& p, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, int num_sms, cudaStream_t stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdk, const CUtensorMap& tdv, int num_sms,
+                            cudaStream_t stream);
 
 }  // namespace fattn
