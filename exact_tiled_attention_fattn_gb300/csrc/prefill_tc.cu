@@ -100,21 +100,24 @@ constexpr float kLazyRescaleLog2 = 8.0f;          // keep m while new scores exc
 // clipped to the blocks the tile visits), with the kept-block counts and the
 // highest and lowest blocks either tile keeps. Producer, MMA issuer and softmax warps walk
 // the bits from shared memory, so no mask load sits on their paths.
-constexpr int kMaskSlots = 4;
+constexpr int kMaskSlots = 3;  // three, so that the epilogue's staging slots fit beside the ring
 constexpr int kMaskWords = 64;                        // up to 2048 blocks per row
 constexpr int kMaskSlotBytes = 2 * kMaskWords * 4 + 16;
 constexpr int kMaskConsumers = 1 + 1 + 8;             // producer, MMA issuer, 8 softmax warps
 static_assert(kMaskWords * 32 == kSparseMaxBlocks, "mask ring size");
 
 // barrier slots (KvFull / KvEmpty: one pair per K/V ring slot, which holds the K tile
-// and the V tile of one step; room for up to kKvSlotsMax slots)
+// and the V tile of one step; room for up to kKvSlotsMax slots; MaskFull / MaskEmpty:
+// room for up to kMaskSlotsMax block-mask slots)
 constexpr int kKvSlotsMax = 3;
+constexpr int kMaskSlotsMax = 4;
+static_assert(kMaskSlots <= kMaskSlotsMax, "mask ring barriers");
 enum : int {
   kBarQFull = 0, kBarQEmpty = 1, kBarKvFull = 2, kBarKvEmpty = 2 + kKvSlotsMax,
   kBarSFull = 2 + 2 * kKvSlotsMax, kBarPFull = kBarSFull + 2, kBarOFull = kBarPFull + 2, kBarMmaDone = kBarOFull + 2,
-  kBarMaskFull = kBarMmaDone + 1, kBarMaskEmpty = kBarMaskFull + kMaskSlots,
+  kBarMaskFull = kBarMmaDone + 1, kBarMaskEmpty = kBarMaskFull + kMaskSlotsMax,
   // separate P buffers (dense d = 64): S_t read by the softmax, O_t += P_t V completed
-  kBarSFree = kBarMaskFull + 2 * kMaskSlots, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
+  kBarSFree = kBarMaskFull + 2 * kMaskSlotsMax, kBarPvDone = kBarSFree + 2, kBarCount = kBarPvDone + 2
 };
 
 enum : int { kModeDense = 0, kModeSparse = 1, kModePaged = 2, kModeMasked = 3, kModeFp8 = 4 };
@@ -137,13 +140,11 @@ struct TcLayout {
   static constexpr int kOffQ = 0;                 // Q_A then Q_B
   static constexpr int kOffK = kOffQ + 2 * kQBytes;
   static constexpr int kOffV = kOffK + kStages * kKVBytes;
-  // Epilogue staging (every variant but the block-sparse one, whose mask ring takes the
-  // room): each softmax warp writes its 32 rows of one 64-column half of O (bf16, 128-byte
-  // swizzle) into a 4 KB slot of its own and stores them with one TMA box.
-  static constexpr bool kStageO = kMode != kModeSparse;
+  // Epilogue staging: each softmax warp writes its 32 rows of one 64-column half of O (bf16,
+  // 128-byte swizzle) into a 4 KB slot of its own and stores them with one TMA box.
   static constexpr int kStageSlot = 32 * 128;
   static constexpr int kOffStage = kOffV + kStages * kKVBytes;
-  static constexpr int kOffBar = kOffStage + (kStageO ? 8 * kStageSlot : 0);
+  static constexpr int kOffBar = kOffStage + 8 * kStageSlot;
   static constexpr int kNumBars = kEarly ? kBarCount : kBarSFree;
   static constexpr int kBarStall = kNumBars;      // test hook: a barrier no role arrives on
   static constexpr int kOffHolder = kOffBar + (kNumBars + 1) * 8;
@@ -341,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    if constexpr (Lay::kStageO) tma_prefetch_desc(&to);
+    tma_prefetch_desc(&to);
   }
   if (warp == 1) {
     tmem_alloc(sb + Lay::kOffHolder, kTmemCols);
@@ -1084,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a row the mask left with no key: O = 0, lse = -inf
       const float inv = (kMasked && l == 0.f) ? 0.f : (kFp8 ? p.v_descale : 1.f) / l;
       const int wrow0 = x.base + t * BM + q4 * 32;  // this warp's first row
-      if (Lay::kStageO && wrow0 + 32 <= x.L) {
+      if (wrow0 + 32 <= x.L) {
         // all 32 rows of the warp lie in the sequence: stage each 64-column half in the
         // warp's slot (row `lane` at 128 lane, 16-byte chunk c at c ^ (lane mod 8): the
         // 128-byte swizzle of the O tensor map) and store it with one TMA box
@@ -1143,7 +1144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // the epilogue's TMA stores complete before the CTA (and its staging slots) goes away
-  if (Lay::kStageO && warp >= 4 && lane == 0) bulk_wait_all();
+  if (warp >= 4 && lane == 0) bulk_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
